@@ -1,0 +1,196 @@
+/*
+ * fanout.h -- C ABI of the shared-prefix fan-out attention library
+ * (libfanout.so, CUDA, sm_103a / GB300).
+ *
+ * The problem (from "AHBM Agentic Runtime Architecture"):
+ *   section 3.1 "Fan-out context structure": a parent context is forked into
+ *     branches by page table; every branch table is [shared prefix pages] +
+ *     [private suffix pages]; shared pages are referenced, never copied.
+ *   section 3.2 "Sub-agent query batching": the new query rows of all branches
+ *     are concatenated along the row dimension (Q_combined) and run as one
+ *     attention; each row stays independent.
+ *   sections 3.3-3.5: every row's keys are split into sequence shards; each
+ *     shard yields an online-softmax partial (m, l, o); partials of the same
+ *     row are merged with the log-sum-exp rule.
+ * and from "ADR-0060: AHBM GQA Fused Attention kernel (Llama3-70B)":
+ *   TL;DR and section 5.2: per KV head, the G = H_q / H_kv query heads that
+ *     share it are folded into the matrix M dimension (no K/V broadcast);
+ *   section 3: FlashAttention tile sweep with online softmax;
+ *   section 4: FlashDecoding split-KV partials merged by log-sum-exp;
+ *   section 5.4: causal tile classification (all past / all future / partial);
+ *   section 0.5.3: softmax_scale (1/sqrt(d) in the pages' use).
+ *
+ * Conventions for every call:
+ *   - Tensors are plain pointers; the caller allocates and owns them. "dev"
+ *     marks device memory of the current CUDA device, "host" host memory.
+ *   - bf16 is IEEE bfloat16 stored in 16 bits.
+ *   - A call returns FANOUT_OK or an error code; nothing is printed and no
+ *     exception crosses the ABI. Argument errors are found on the host before
+ *     any launch. Errors inside a kernel (a bounded wait that ran out) are
+ *     recorded in a device word and reported by fanout_last_error().
+ *   - Calls are asynchronous with respect to the host unless stated.
+ */
+#ifndef FANOUT_H
+#define FANOUT_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FANOUT_API __attribute__((visibility("default")))
+#else
+#define FANOUT_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream; NULL is the legacy default stream. */
+struct CUstream_st;
+typedef struct CUstream_st *fanout_stream_t;
+struct CUevent_st;
+typedef struct CUevent_st *fanout_event_t;
+
+enum fanout_status {
+    FANOUT_OK = 0,
+    FANOUT_EINVAL = 1,        /* invalid argument (null pointer, bad size, bad page id) */
+    FANOUT_EUNSUPPORTED = 2,  /* valid problem outside what this build supports */
+    FANOUT_ECUDA = 3,         /* a CUDA runtime/driver call failed */
+    FANOUT_ENOMEM = 4,        /* workspace allocation failed */
+    FANOUT_ETIMEOUT = 5       /* a bounded device-side wait ran out */
+};
+
+enum fanout_out_dtype { FANOUT_OUT_F32 = 0, FANOUT_OUT_BF16 = 1 };
+
+/*
+ * fanout_fork -- build branch page tables (host only, no device work).
+ * "AHBM Agentic Runtime Architecture", section 3.1 "Fan-out context structure".
+ *
+ *   prefix_pages   host int32 [n_prefix_pages]: physical ids of the shared
+ *                  prefix pages, in logical order.
+ *   num_branches   B >= 0.
+ *   suffix_lens    host int32 [B]: private suffix length of each branch, tokens.
+ *   page_size      tokens per page (> 0).
+ *   free_pages     host int32 [n_free]: physical ids available for private
+ *                  pages; branch 0 takes the first ceil(S_0/page_size), branch
+ *                  1 the next, and so on.
+ *   page_table     host int32 [B][max_pages_per_branch], written: row b =
+ *                  prefix ids, then branch b's private ids, then -1.
+ * Returns FANOUT_EINVAL on a null pointer, a negative size, a free list too
+ * short, or a row too narrow. On error page_table is left unspecified.
+ */
+FANOUT_API int fanout_fork(const int32_t *prefix_pages, int32_t n_prefix_pages, int32_t num_branches,
+                const int32_t *suffix_lens, int32_t page_size, const int32_t *free_pages,
+                int32_t n_free, int32_t *page_table, int32_t max_pages_per_branch);
+
+/*
+ * fanout_attn -- batched shared-prefix fan-out attention.
+ * "AHBM Agentic Runtime Architecture" sections 3.2-3.5; "ADR-0060" TL;DR,
+ * sections 3, 4, 5.2 and 5.4.
+ *
+ * Rows. R = sum_b q_rows_per_branch[b] query tokens, grouped by branch
+ * (branch 0's T_0 tokens first). Token t of branch b sits at absolute position
+ *   pos = prefix_len + suffix_lens[b] - q_rows_per_branch[b] + t,
+ * i.e. the new tokens are the tail of the branch's private suffix, and their
+ * K/V are already in the pool (the kernel is a pure read of the cache).
+ * Keys. Branch b sees keys 0 .. prefix_len + suffix_lens[b] - 1 of its own
+ * logical sequence; key j lives at
+ *   k_pages[page_table[b][j / page_size]][h_kv][j % page_size][0..d-1].
+ * With causal != 0 key j is visible to the token at pos iff j <= pos.
+ * Query head h uses KV head h / (H_q / H_kv).
+ *
+ *   q                dev bf16 [R][H_q][d] (post-RoPE queries).
+ *   k_pages, v_pages dev bf16 [num_pages][H_kv][page_size][d]. 16-byte aligned.
+ *   page_table       dev int32 [num_branches][max_pages_per_branch]; every
+ *                    entry a branch reads must be in [0, num_pages).
+ *   prefix_len       tokens, a multiple of page_size (>= 0).
+ *   suffix_lens      HOST int32 [num_branches] (>= 0).
+ *   q_rows_per_branch HOST int32 [num_branches] (>= 0); with causal != 0 each
+ *                    must be <= suffix_lens[b].
+ *   H_q, H_kv        H_q % H_kv == 0, G = H_q / H_kv <= 128.
+ *   d                head dimension; this build supports d == 128.
+ *   page_size        one of 16, 32, 64, 128.
+ *   scale            softmax scale applied to q.k (the pages use 1/sqrt(d)).
+ *   out              dev [R][H_q][d], fp32 or bf16 per out_dtype:
+ *                    out = softmax(scale q K^T) V, normalised.
+ *   lse              dev fp32 [R][H_q] or NULL: natural-log log-sum-exp of the
+ *                    scaled visible scores, m + ln(l).
+ *   stream           stream the work is ordered on.
+ * Host-side validation reads only host arrays; page-table entries are read by
+ * the kernel (set option FANOUT_OPT_VALIDATE_TABLE to check them on the host
+ * with a device-to-host copy first). R == 0 is a no-op returning FANOUT_OK.
+ * The library keeps a grow-only device workspace per (device, stream) for
+ * split partials and the work plan; it is freed by fanout_release().
+ */
+FANOUT_API int fanout_attn(const void *q, const void *k_pages, const void *v_pages,
+                const int32_t *page_table, int32_t prefix_len, const int32_t *suffix_lens,
+                const int32_t *q_rows_per_branch, int32_t num_branches,
+                int32_t max_pages_per_branch, int32_t num_pages, int32_t H_q, int32_t H_kv,
+                int32_t d, int32_t page_size, float scale, int32_t causal, void *out,
+                int32_t out_dtype, float *lse, fanout_stream_t stream);
+
+/*
+ * fanout_lse_merge -- the log-sum-exp merge of split partials on its own
+ * (ADR-0060 section 4 "Reduction"; "AHBM Agentic Runtime Architecture"
+ * section 3.4). For every output n (n < n_out) fold parts p = 0 .. n_parts-1
+ * in ascending order:
+ *   m_p   = part_ml[p][n].x  (running max, base-2 domain: max of scale*log2(e)*s)
+ *   l_p   = part_ml[p][n].y  (sum of 2^(x - m_p))
+ *   o_p   = part_o[p][n][0..d-1] (unnormalised)
+ * out[n] = sum_p 2^(m_p - M) o_p / L,  L = sum_p 2^(m_p - M) l_p, M = max_p m_p;
+ * lse[n] = (M + log2 L) * ln 2. A part with l_p == 0 (no visible key) weighs 0.
+ *   part_o dev fp32 [n_parts][n_out][d]; part_ml dev fp32 [n_parts][n_out][2];
+ *   out dev [n_out][d] (fp32/bf16), lse dev fp32 [n_out] or NULL.
+ * This is the merge step fanout_attn runs internally, exposed for testing.
+ */
+FANOUT_API int fanout_lse_merge(const float *part_o, const float *part_ml, int32_t n_parts, int64_t n_out,
+                     int32_t d, void *out, int32_t out_dtype, float *lse, fanout_stream_t stream);
+
+/* Synchronises `stream`, then returns and clears the device error word of the
+ * current device: FANOUT_OK, FANOUT_ETIMEOUT, or FANOUT_ECUDA when the stream
+ * itself reports a CUDA error. */
+FANOUT_API int fanout_last_error(fanout_stream_t stream);
+
+/* Static text for a status code (never NULL). */
+FANOUT_API const char *fanout_strerror(int code);
+
+/* Tuning / diagnostics options (process-wide; set before the calls they affect). */
+enum fanout_option {
+    FANOUT_OPT_SPLITS = 1,          /* >0: force this many key splits per row tile; 0 = auto */
+    FANOUT_OPT_VALIDATE_TABLE = 2,  /* 1: check page-table entries on the host each call */
+    FANOUT_OPT_WAIT_LIMIT_NS = 3,   /* bound of every device-side wait (default 1e9 ns) */
+    FANOUT_OPT_NUM_SMS = 4          /* >0: plan for this many SMs instead of the device's */
+};
+FANOUT_API int fanout_set_option(int32_t option, int64_t value);
+
+/* Record `before` / `after` on the call's stream around the split-KV attention
+ * kernel of every following fanout_attn call (NULL, NULL turns it off). Used to
+ * time that kernel alone. */
+FANOUT_API int fanout_set_profile_events(fanout_event_t before, fanout_event_t after);
+
+/* Host-side description of the work plan fanout_attn would run for a problem
+ * (no device access). Writes up to `cap` unit records of 8 int32 each:
+ *   {kv_head, branch, tok_begin, n_tok, key_begin, key_end, pos_base, slot}
+ * (see the split-KV kernel), and the counts. Returns FANOUT_OK or an error
+ * code with the same validation as fanout_attn. */
+FANOUT_API int fanout_plan(const int32_t *suffix_lens, const int32_t *q_rows_per_branch,
+                int32_t num_branches, int32_t prefix_len, int32_t H_q, int32_t H_kv,
+                int32_t page_size, int32_t causal, int32_t num_sms, int32_t *units,
+                int32_t cap, int32_t *n_units, int32_t *n_slots, int32_t *tok_slots);
+
+/* Launches one tiny kernel whose single thread waits on a barrier nothing ever
+ * completes, bounded by `limit_ns`; returns FANOUT_ETIMEOUT when the bound
+ * fires and the kernel came back (the context stays usable), FANOUT_OK never
+ * (a completed wait would be a bug). Tests the bounded-wait path. */
+FANOUT_API int fanout_selftest_wait_timeout(int64_t limit_ns, fanout_stream_t stream);
+
+/* Frees the workspaces of every device and stream (synchronises first). */
+FANOUT_API int fanout_release(void);
+
+/* Library version, "major.minor.patch". */
+FANOUT_API const char *fanout_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FANOUT_H */

@@ -1,0 +1,133 @@
+"""GPU invariants the pages fix: determinism, page-placement invariance,
+batching invariance, split invariance, one-token causal == non-causal,
+identical keys -> mean of V; plus the merge kernel against the oracle's merge
+and the edge cases (empty problem, branches without rows)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from shared_prefix_fan_gb300 import binding
+from shared_prefix_fan_gb300.workloads import WORKLOADS, draw, small_spec
+from tests.gpu_helpers import DevWorkload, compare, oracle_ref, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+
+
+def test_deterministic_bitwise():
+    dw = DevWorkload(draw(WORKLOADS["batching"]))
+    o0, l0 = dw.run()
+    for _ in range(2):
+        o, l = dw.run()
+        assert torch.equal(o, o0) and torch.equal(l, l0)
+
+
+def test_page_placement_bitwise():
+    w = draw(small_spec(h_q=16, h_kv=2, page_size=16, prefix_len=512, q_rows=[4, 9],
+                        suffix_lens=[70, 300], seed=9))
+    dw = DevWorkload(w)
+    o0, l0 = dw.run()
+    n = dw.k.shape[0]
+    perm = torch.randperm(n, generator=torch.Generator().manual_seed(1))
+    inv = torch.argsort(perm)
+    k2, v2 = dw.k[perm.cuda()].contiguous(), dw.v[perm.cuda()].contiguous()
+    t = dw.table.long()
+    t2 = torch.where(t >= 0, inv.cuda()[t.clamp(min=0)], t).to(torch.int32).contiguous()
+    o1, l1 = dw.run(table=t2, k=k2, v=v2)
+    assert torch.equal(o0, o1) and torch.equal(l0, l1)
+
+
+def test_batched_equals_per_branch():
+    w = draw(small_spec(h_q=64, h_kv=8, page_size=64, prefix_len=2048, q_rows=[5, 20, 1, 12],
+                        suffix_lens=[64, 256, 100, 12], seed=12))
+    dw = DevWorkload(w)
+    ob, lb = dw.run()
+    r0 = 0
+    for b in range(w.num_branches):
+        T = int(w.q_rows[b])
+        s = w.spec
+        o, l = binding.attn(dw.q[r0:r0 + T].contiguous(), dw.k, dw.v,
+                            dw.table[b:b + 1].contiguous(), s.prefix_len, [w.suffix_lens[b]], [T],
+                            s.h_q, s.h_kv, s.page_size, s.scale, s.causal)
+        assert binding.last_error() == binding.OK
+        d = (o - ob[r0:r0 + T]).abs().max().item()
+        assert d <= 2e-3, d
+        assert (l - lb[r0:r0 + T]).abs().max().item() <= 1e-4
+        r0 += T
+
+
+def test_split_invariance():
+    dw = DevWorkload(draw(WORKLOADS["decode"]))
+    try:
+        binding.set_option(binding.OPT_SPLITS, 1)
+        o1, l1 = dw.run()
+        binding.set_option(binding.OPT_SPLITS, 7)
+        o7, l7 = dw.run()
+    finally:
+        binding.set_option(binding.OPT_SPLITS, 0)
+    assert (o1 - o7).abs().max().item() <= 1e-4
+    assert (l1 - l7).abs().max().item() <= 1e-4
+
+
+def test_single_token_causal_equals_noncausal():
+    dw = DevWorkload(draw(WORKLOADS["decode"]))
+    oc, lc = dw.run(causal=True)
+    on, ln = dw.run(causal=False)
+    assert torch.equal(oc, on) and torch.equal(lc, ln)
+
+
+def test_identical_keys_give_mean_of_v():
+    spec = small_spec(h_q=8, h_kv=1, page_size=16, prefix_len=256, q_rows=[3, 5],
+                      suffix_lens=[40, 77], seed=4)
+    w = draw(spec)
+    w.k_pool[:] = w.k_pool[0, 0, 0][None, None, None, :]
+    dw = DevWorkload(w)
+    out, lse = dw.run()
+    table = dw.table_host
+    ps, P = spec.page_size, spec.prefix_len
+    from shared_prefix_fan_gb300.workloads import bf16_bits_to_f32
+    v = bf16_bits_to_f32(w.v_pool).astype(np.float64)
+    r = 0
+    for b in range(w.num_branches):
+        n_all = P + int(w.suffix_lens[b])
+        for t in range(int(w.q_rows[b])):
+            n_vis = n_all - int(w.q_rows[b]) + t + 1
+            keys = np.arange(n_vis)
+            vs = v[table[b, keys // ps], 0, keys % ps]
+            got = out[r].double().cpu().numpy()
+            assert np.abs(got - vs.mean(0)[None]).max() <= 2e-3
+            r += 1
+
+
+def test_merge_kernel_matches_oracle_merge():
+    rng = np.random.default_rng(0)
+    n_parts, n, d = 5, 300, 128
+    m = rng.normal(0, 3, size=(n_parts, n))
+    l = rng.uniform(0.5, 40, size=(n_parts, n))
+    l[1, ::7] = 0.0          # empty shards
+    m[1, ::7] = -np.inf
+    o = rng.normal(size=(n_parts, n, d)) * l[..., None]
+    ml = np.stack([m / np.log(2), l], -1).astype(np.float32)   # kernel keeps m in log2 units
+    po = torch.from_numpy(o.astype(np.float32)).cuda()
+    pml = torch.from_numpy(ml).cuda()
+    out, lse = binding.lse_merge(po, pml)
+    torch.cuda.synchronize()
+    # oracle on the fp32-rounded partials, natural-log domain
+    m32 = ml[..., 0].astype(np.float64) * np.log(2)
+    ro, rl = oracle.merge(m32, ml[..., 1].astype(np.float64), o.astype(np.float32).astype(np.float64))
+    assert np.abs(out.double().cpu().numpy() - ro).max() <= 1e-5
+    assert np.abs(lse.double().cpu().numpy() - rl).max() <= 1e-5
+
+
+def test_empty_and_rowless_branches():
+    spec = small_spec(h_q=8, h_kv=2, page_size=16, prefix_len=64, q_rows=[0, 0],
+                      suffix_lens=[5, 9], seed=2)
+    w = draw(spec)
+    dw = DevWorkload(w)
+    out, lse = dw.run()
+    assert out.shape[0] == 0
+    spec = small_spec(h_q=8, h_kv=2, page_size=16, prefix_len=64, q_rows=[0, 6, 0],
+                      suffix_lens=[5, 9, 30], seed=3)
+    w = draw(spec)
+    out, lse = DevWorkload(w).run()
+    compare(out, lse, *oracle_ref(w), what="row-less branches")

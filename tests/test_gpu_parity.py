@@ -1,0 +1,92 @@
+"""GPU parity: fanout_attn (through the C ABI) against the fp64 oracle on the
+same seeded inputs, element by element. Five workloads at full size (the two
+largest checked on sampled rows the oracle computes one by one), a sweep of
+small shapes spanning several tiles and ragged tails, and edge cases."""
+import numpy as np
+import pytest
+import torch
+
+from shared_prefix_fan_gb300 import binding
+from shared_prefix_fan_gb300.workloads import WORKLOADS, draw, small_spec
+from tests.gpu_helpers import DevWorkload, compare, oracle_ref, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+def test_wait_timeout_reports_and_context_survives():
+    DevWorkload(draw(WORKLOADS["tiny"]))  # builds/loads the library
+    assert binding.selftest_wait_timeout(20_000_000) == binding.ETIMEOUT
+    assert binding.last_error() == binding.OK  # cleared
+    w = draw(WORKLOADS["tiny"])
+    out, lse = DevWorkload(w).run()
+    compare(out, lse, *oracle_ref(w), what="tiny after timeout")
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode", "batching"])
+def test_full_workload(name):
+    w = draw(WORKLOADS[name])
+    out, lse = DevWorkload(w).run()
+    compare(out, lse, *oracle_ref(w), what=name)
+
+
+@pytest.mark.parametrize("name,every", [("wide", 16), ("prefill", 512)])
+def test_large_workload_sampled(name, every):
+    w = draw(WORKLOADS[name])
+    rows = sample_rows(w, every)
+    out, lse = DevWorkload(w).run()
+    ref_o, ref_l = oracle_ref(w, rows=rows)
+    compare(out, lse, ref_o, ref_l, rows=rows, what=name)
+    assert torch.isfinite(out).all() and torch.isfinite(lse).all()
+
+
+SWEEP = [
+    # (q_rows, suffix_lens, prefix, page, h_q, h_kv, causal)
+    ([1], [1], 0, 16, 8, 8, True),
+    ([2, 7], [9, 40], 32, 16, 8, 2, True),
+    ([16, 33, 1], [100, 33, 500], 256, 64, 16, 2, True),
+    ([33], [300], 0, 64, 4, 1, True),
+    ([7, 7, 7, 7], [7, 90, 129, 128], 128, 32, 32, 4, True),
+    ([5, 3], [17, 3], 16, 16, 8, 1, False),
+    ([40, 0, 12], [600, 10, 12], 1024, 128, 64, 8, True),
+    ([1] * 9, [200] * 9, 2048, 16, 64, 8, True),
+    ([20, 20], [256, 256], 512, 64, 128, 1, True),   # G = 128: one token per tile
+    ([3, 4], [0, 4], 64, 16, 8, 2, False),            # a branch with no private suffix
+]
+
+
+@pytest.mark.parametrize("case", range(len(SWEEP)))
+def test_small_sweep(case):
+    tq, sl, P, ps, hq, hkv, causal = SWEEP[case]
+    spec = small_spec(h_q=hq, h_kv=hkv, page_size=ps, prefix_len=P, causal=causal,
+                      q_rows=tq, suffix_lens=sl, permute_prefix=True, permute_suffix=True,
+                      seed=100 + case)
+    w = draw(spec)
+    out, lse = DevWorkload(w).run()
+    compare(out, lse, *oracle_ref(w), what=f"sweep {case}")
+
+
+@pytest.mark.parametrize("splits", [1, 2, 3, 32])
+def test_forced_splits(splits):
+    spec = small_spec(h_q=16, h_kv=2, page_size=16, prefix_len=1024, q_rows=[3, 9, 1],
+                      suffix_lens=[200, 45, 700], seed=55)
+    w = draw(spec)
+    dw = DevWorkload(w)
+    ref = oracle_ref(w)
+    try:
+        binding.set_option(binding.OPT_SPLITS, splits)
+        out, lse = dw.run()
+    finally:
+        binding.set_option(binding.OPT_SPLITS, 0)
+    compare(out, lse, *ref, what=f"splits={splits}")
+
+
+def test_bf16_output():
+    w = draw(WORKLOADS["batching"])
+    out, lse = DevWorkload(w).run(out_dtype="bf16")
+    ref_o, ref_l = oracle_ref(w)
+    # the oracle rounded to bf16 (round to nearest even) is what a perfect kernel writes
+    ref_bf = torch.from_numpy(ref_o).float().to(torch.bfloat16).double().numpy()
+    o = out.double().cpu().numpy()
+    ulp = np.abs(ref_bf) * 2.0 ** -8 + 1e-30
+    assert (np.abs(o - ref_bf) <= ulp + 2e-3).all()
+    compare(out, lse, ref_o, ref_l, what="bf16 out")

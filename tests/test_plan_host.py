@@ -1,0 +1,111 @@
+"""The host work planner: every visible key of every (token, query head) is
+covered by exactly one unit, partial slots are consistent, and the planned
+work equals the visible-pair count (the pages' compute identity) (CPU only)."""
+import numpy as np
+import pytest
+
+import oracle
+from shared_prefix_fan_gb300 import binding, build
+from shared_prefix_fan_gb300.workloads import WORKLOADS, draw
+
+NO_CAUSAL = 1 << 30
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build.build()
+
+
+def check_plan(S, T, P, h_q, h_kv, ps, causal, sms=148):
+    S, T = list(map(int, S)), list(map(int, T))
+    units, n_slots, tok_slots = binding.plan(S, T, P, h_q, h_kv, ps, causal, sms)
+    G = h_q // h_kv
+    R = sum(T)
+    tok_branch = np.repeat(np.arange(len(T)), T)
+    tok0 = np.concatenate([[0], np.cumsum(T)])
+    vis = np.zeros(R, dtype=np.int64)
+    pos = np.zeros(R, dtype=np.int64)
+    for r in range(R):
+        b = tok_branch[r]
+        pos[r] = P + S[b] - T[b] + (r - tok0[b])
+        vis[r] = min(P + S[b], pos[r] + 1) if causal else P + S[b]
+    covered = {}   # (r, h) -> list of (lo, hi, slot)
+    total_pairs = 0
+    for row in units:
+        h, br, tb, nt, k0, k1, pb, slot = (int(x) for x in row)
+        assert k1 > k0 >= 0 and nt >= 1 and nt * G <= 128 and 0 <= h < h_kv
+        assert k0 % ps == 0, "chunk start not page aligned"
+        for r in range(tb, tb + nt):
+            b = int(tok_branch[r])
+            if k1 > P:   # touches private keys: single-branch unit, through its own table
+                assert br == b
+            if pb != NO_CAUSAL:
+                assert pb + r == pos[r], "causal position mismatch"
+            else:
+                assert not causal or k1 <= P, "an unmasked unit reaches past the prefix"
+            hi = min(k1, int(vis[r]))
+            covered.setdefault((r, h), []).append((k0, max(hi, k0), slot))
+            total_pairs += max(0, hi - k0) * G
+    for r in range(R):
+        for h in range(h_kv):
+            segs = sorted(covered.get((r, h), []))
+            assert segs, f"token {r} head {h} uncovered"
+            # contiguous, disjoint cover of [0, vis)
+            cur = 0
+            for lo, hi, _ in segs:
+                assert lo == cur or hi <= lo, (r, h, segs)
+                cur = max(cur, hi)
+            assert cur == vis[r], (r, h, segs, vis[r])
+            slots = sorted(s for _, _, s in segs)
+            if tok_slots[r] == 0:
+                assert slots == [-1]
+            else:
+                assert slots == list(range(tok_slots[r])), (r, slots, tok_slots[r])
+    assert n_slots == (max(tok_slots) if R else 0)
+    assert total_pairs == oracle.count_pairs(P, S, T, h_q, causal)
+    return units, n_slots, tok_slots
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode", "batching", "wide"])
+def test_plan_workloads(name):
+    w = draw(WORKLOADS[name]) if name != "wide" else draw(WORKLOADS[name])
+    s = w.spec
+    check_plan(w.suffix_lens, w.q_rows, s.prefix_len, s.h_q, s.h_kv, s.page_size, s.causal)
+
+
+def test_plan_prefill_is_direct():
+    s = WORKLOADS["prefill"]
+    units, n_slots, tok_slots = binding.plan(s.suffix_lens, s.q_rows, s.prefix_len, s.h_q,
+                                             s.h_kv, s.page_size, s.causal, 148)
+    assert n_slots == 0 and (tok_slots == 0).all() and (units[:, 7] == -1).all()
+    assert len(units) == 8 * 8192 // 16
+
+
+def test_plan_decode_split_32():
+    s = WORKLOADS["decode"]
+    units, n_slots, _ = binding.plan(s.suffix_lens, s.q_rows, s.prefix_len, s.h_q, s.h_kv,
+                                     s.page_size, s.causal, 152)
+    prefix_units = units[units[:, 5] <= s.prefix_len]
+    assert len(prefix_units) == 8 * 32   # 8 KV heads x 32 key splits of the shared prefix
+    assert n_slots == 33
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_plan_random(seed):
+    rng = np.random.default_rng(seed)
+    B = int(rng.integers(1, 6))
+    ps = int(rng.choice([16, 32, 64, 128]))
+    P = ps * int(rng.integers(0, 12))
+    causal = bool(rng.integers(0, 2))
+    T = rng.integers(0, 40, size=B)
+    S = np.array([int(t) + int(rng.integers(0 if P else 1, 300)) for t in T])
+    if not causal:
+        S = rng.integers(0 if P else 1, 300, size=B)
+    hkv = int(rng.choice([1, 2, 8]))
+    hq = hkv * int(rng.choice([1, 3, 8, 16]))
+    sms = int(rng.choice([1, 7, 148]))
+    try:
+        binding.set_option(binding.OPT_SPLITS, int(rng.choice([0, 0, 1, 3])))
+        check_plan(S, T, P, hq, hkv, ps, causal, sms)
+    finally:
+        binding.set_option(binding.OPT_SPLITS, 0)
