@@ -184,6 +184,39 @@ FANOUT_API int fanout_plan(const int32_t *suffix_lens, const int32_t *q_rows_per
  * (a completed wait would be a bug). Tests the bounded-wait path. */
 FANOUT_API int fanout_selftest_wait_timeout(int64_t limit_ns, fanout_stream_t stream);
 
+/*
+ * fanout_attn_noalloc -- fanout_attn that allocates no device memory.
+ * The pages have no counterpart: this entry exists for callers of this
+ * library that must not allocate device memory during a call -- a serving
+ * engine that has reserved the device's memory for its own pool, code that
+ * cannot afford the device-wide synchronisation of cudaFree, or code running
+ * where allocation is not allowed. fanout_attn obtains its workspace with
+ * cudaMalloc; this entry instead keeps the work plan and the split-KV partials
+ * in one fixed array of FANOUT_NOALLOC_SCRATCH_BYTES compiled into the library
+ * (every GPU that loads the library holds it until the process exits).
+ * Arguments, layouts and results are those of fanout_attn (same kernels, same
+ * plan, so the same output); the caller still allocates q, the pools, the
+ * page table, out and lse. Differences:
+ *   - FANOUT_ENOMEM, before anything runs, when the problem's plan plus
+ *     partials need more than FANOUT_NOALLOC_SCRATCH_BYTES;
+ *   - the first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture;
+ *   - all calls share the one array, and it keeps the last call's contents.
+ *     Nothing in it needs clearing (each call writes all it reads), but calls
+ *     that overlap on the GPU (two streams, or a new call before the previous
+ *     one finished) race on it and corrupt each other's results;
+ *   - FANOUT_OPT_WAIT_LIMIT_NS and FANOUT_OPT_NUM_SMS do not apply (1 s bound,
+ *     the device's own SM count); profile events are not recorded.
+ */
+#define FANOUT_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+FANOUT_API int fanout_attn_noalloc(const void *q, const void *k_pages, const void *v_pages,
+                const int32_t *page_table, int32_t prefix_len, const int32_t *suffix_lens,
+                const int32_t *q_rows_per_branch, int32_t num_branches,
+                int32_t max_pages_per_branch, int32_t num_pages, int32_t H_q, int32_t H_kv,
+                int32_t d, int32_t page_size, float scale, int32_t causal, void *out,
+                int32_t out_dtype, float *lse, fanout_stream_t stream);
+
 /* Frees the workspaces of every device and stream (synchronises first). */
 FANOUT_API int fanout_release(void);
 

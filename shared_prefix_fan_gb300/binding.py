@@ -27,6 +27,9 @@ ABI = {
     "fanout_fork": (ctypes.c_int, [_i32p, _i32, _i32, _i32p, _i32, _i32p, _i32, _i32p, _i32]),
     "fanout_attn": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _i32p, _i32p, _i32, _i32, _i32, _i32,
                                    _i32, _i32, _i32, _f32, _i32, _vp, _i32, _vp, _vp]),
+    "fanout_attn_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _i32p, _i32p, _i32, _i32,
+                                           _i32, _i32, _i32, _i32, _i32, _f32, _i32, _vp, _i32,
+                                           _vp, _vp]),
     "fanout_lse_merge": (ctypes.c_int, [_vp, _vp, _i32, _i64, _i32, _vp, _i32, _vp, _vp]),
     "fanout_last_error": (ctypes.c_int, [_vp]),
     "fanout_strerror": (ctypes.c_char_p, [ctypes.c_int]),
@@ -168,6 +171,28 @@ def attn(q, k_pages, v_pages, page_table, prefix_len: int, suffix_lens: Sequence
                          lse.data_ptr() if lse is not None else None, _stream_handle(stream))
     _check(rc, "fanout_attn")
     return out, lse
+
+
+# Fixed scratch of fanout_attn_noalloc (FANOUT_NOALLOC_SCRATCH_BYTES in include/fanout.h).
+NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
+
+
+def attn_noalloc(q, k_pages, v_pages, page_table, prefix_len: int, suffix_lens, q_rows,
+                 h_q: int, h_kv: int, page_size: int, scale: float, causal: bool, out, lse,
+                 out_dtype: str = "f32", stream=None) -> int:
+    """fanout_attn_noalloc: same call as attn() into caller-allocated out/lse,
+    for callers that must not allocate device memory during a call (the library
+    uses its fixed scratch array instead of a cudaMalloc'd workspace). Returns
+    the status code (FANOUT_ENOMEM when the problem needs more scratch than the
+    fixed array holds) instead of raising, and allocates nothing itself."""
+    sl, tq = _i32arr(suffix_lens), _i32arr(q_rows)
+    odt = {"f32": OUT_F32, "bf16": OUT_BF16}[out_dtype]
+    return int(load().fanout_attn_noalloc(
+        q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(), page_table.data_ptr(),
+        int(prefix_len), _ptr(sl), _ptr(tq), int(sl.shape[0]), int(page_table.shape[1]),
+        int(k_pages.shape[0]), int(h_q), int(h_kv), int(q.shape[-1]), int(page_size),
+        float(scale), int(bool(causal)), out.data_ptr(), odt,
+        lse.data_ptr() if lse is not None else None, _stream_handle(stream)))
 
 
 def lse_merge(part_o, part_ml, out=None, lse=None, out_dtype: str = "f32", stream=None):

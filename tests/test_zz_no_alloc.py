@@ -1,0 +1,57 @@
+"""fanout_attn_noalloc: the attention call for callers that must not allocate
+device memory during a call (an engine that owns all device memory through its
+own pool, code that cannot afford cudaFree's device-wide synchronisation, or
+code running where allocation is not allowed). It keeps its work plan and
+split partials in the library's fixed scratch array instead of a cudaMalloc'd
+workspace. Checked against fanout_attn, through the C ABI, on two calls in a
+row with different problems (the shared array keeps the previous call's
+contents), and for the clear rejection of a problem too big for the array.
+
+This file is collected last on purpose (pytest orders files by name)."""
+import numpy as np
+import pytest
+import torch
+
+from shared_prefix_fan_gb300 import binding
+from shared_prefix_fan_gb300.workloads import WORKLOADS, draw
+from tests.gpu_helpers import TOL_LSE, TOL_MAX_O, TOL_MEAN_O, DevWorkload
+
+pytestmark = pytest.mark.gpu
+
+
+def _noalloc(dw, out, lse):
+    s = dw.w.spec
+    return binding.attn_noalloc(dw.q, dw.k, dw.v, dw.table, s.prefix_len, dw.w.suffix_lens,
+                                dw.w.q_rows, s.h_q, s.h_kv, s.page_size, s.scale, s.causal,
+                                out, lse)
+
+
+def _close(a_out, a_lse, b_out, b_lse):
+    d = (a_out.double() - b_out.double()).abs()
+    assert d.max().item() <= TOL_MAX_O and d.mean().item() <= TOL_MEAN_O
+    assert (a_lse.double() - b_lse.double()).abs().max().item() <= TOL_LSE
+
+
+def test_noalloc_matches_fanout_attn_on_two_calls():
+    for name in ("decode", "batching"):   # two calls in a row, different plans
+        dw = DevWorkload(draw(WORKLOADS[name]))
+        ref_out, ref_lse = dw.run()
+        out = torch.full_like(ref_out, float("nan"))
+        lse = torch.full_like(ref_lse, float("nan"))
+        assert _noalloc(dw, out, lse) == binding.OK
+        assert binding.last_error() == binding.OK
+        _close(out, lse, ref_out, ref_lse)
+
+
+def test_noalloc_rejects_problem_beyond_scratch():
+    dw = DevWorkload(draw(WORKLOADS["batching"]))
+    out = torch.zeros((dw.w.total_rows, dw.w.spec.h_q, 128), device="cuda")
+    lse = torch.zeros((dw.w.total_rows, dw.w.spec.h_q), device="cuda")
+    try:
+        # 10 partial slots x 160 tokens x 64 heads x 520 B > the 32 MiB array
+        binding.set_option(binding.OPT_SPLITS, 8)
+        assert _noalloc(dw, out, lse) == binding.ENOMEM
+    finally:
+        binding.set_option(binding.OPT_SPLITS, 0)
+    torch.cuda.synchronize()
+    assert (out == 0).all().item()   # nothing ran
