@@ -33,7 +33,7 @@ sys.path.insert(0, ROOT)
 from shared_prefix_fan_gb300.workloads import WORKLOADS, draw  # noqa: E402
 
 METRIC = "us/call and achieved roofline % (KV HBM GB/s or tensor TFLOP/s) per config"
-KERNEL_SOURCES = ["split_attn.cu", "ptx_sm100.cuh", "fanout_internal.h"]
+KERNEL_SOURCES = ["attn_fwd.cu", "ptx_sm100.cuh", "fanout_internal.h"]
 
 
 # ------------------------------------------------------------------ accounting
@@ -284,10 +284,10 @@ def main():
     rc = binding.last_error()
     if rc != binding.OK:
         raise RuntimeError(f"device error {binding.strerror(rc)}")
-    units, n_slots, tok_slots = binding.plan(w.suffix_lens, w.q_rows, s.prefix_len, s.h_q,
-                                             s.h_kv, s.page_size, s.causal,
-                                             torch.cuda.get_device_properties(local).multi_processor_count)
-    launches_per_call = 1 + (1 if n_slots > 0 else 0)
+    units, cta_first, n_parts = binding.plan(
+        w.suffix_lens, w.q_rows, s.prefix_len, s.h_q, s.h_kv, s.page_size, s.causal,
+        torch.cuda.get_device_properties(local).multi_processor_count)
+    launches_per_call = 1 + (1 if n_parts > 0 else 0)
 
     sampler = ClockSampler(gpu_id_for_smi(torch, local))
     t_end = time.perf_counter() + args.soak_s
@@ -377,7 +377,7 @@ def main():
         roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["tc"], "unit": "TFLOP/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["traffic"] = ncu_traffic(args.config)
-    roof["kernel"] = "split_attn_kernel"
+    roof["kernel"] = "attn_fwd_kernel"
     roof["peak_source"] = f"{peaks['source']} (MEASURED_PEAKS.json burst figure)" \
         if peaks["source"] == "measured" else "fallback"
     t_call_roof = max(work["call_bytes"] / (peaks["hbm"] * 1e9), t_tc)
@@ -398,7 +398,8 @@ def main():
         "config": {"workload": args.config, "h_q": s.h_q, "h_kv": s.h_kv, "d": s.d,
                    "branches": w.num_branches, "q_rows": int(R), "prefix_len": s.prefix_len,
                    "suffix_tokens": int(w.suffix_lens.sum()), "page_size": s.page_size,
-                   "causal": s.causal, "work_units": int(len(units)), "partial_slots": n_slots,
+                   "causal": s.causal, "work_units": int(len(units)),
+                   "persistent_ctas": int(len(cta_first) - 1), "partial_blocks": n_parts,
                    "l2": "flushed between timed calls (memset of 2x L2)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "call_roofline": {"t_roof_us": t_call_roof * 1e6, "frac": t_call_roof / (value_us * 1e-6),

@@ -110,7 +110,8 @@ FANOUT_API int fanout_fork(const int32_t *prefix_pages, int32_t n_prefix_pages, 
  *   H_q, H_kv        H_q % H_kv == 0, G = H_q / H_kv <= 128.
  *   d                head dimension; this build supports d == 128.
  *   page_size        one of 16, 32, 64, 128.
- *   scale            softmax scale applied to q.k (the pages use 1/sqrt(d)).
+ *   scale            softmax scale applied to q.k, finite and > 0 (the pages
+ *                    use 1/sqrt(d)).
  *   out              dev [R][H_q][d], fp32 or bf16 per out_dtype:
  *                    out = softmax(scale q K^T) V, normalised.
  *   lse              dev fp32 [R][H_q] or NULL: natural-log log-sum-exp of the
@@ -151,12 +152,17 @@ FANOUT_API int fanout_lse_merge(const float *part_o, const float *part_ml, int32
  * itself reports a CUDA error. */
 FANOUT_API int fanout_last_error(fanout_stream_t stream);
 
+/* fanout_last_error, also reporting where a device-side wait gave up: `site`
+ * (an internal wait-site number of the kernel) and `block` (CTA index); both
+ * may be NULL and are 0 when no error was recorded. */
+FANOUT_API int fanout_last_error_detail(fanout_stream_t stream, int32_t *site, int32_t *block);
+
 /* Static text for a status code (never NULL). */
 FANOUT_API const char *fanout_strerror(int code);
 
 /* Tuning / diagnostics options (process-wide; set before the calls they affect). */
 enum fanout_option {
-    FANOUT_OPT_SPLITS = 1,          /* >0: force this many key splits per row tile; 0 = auto */
+    FANOUT_OPT_SPLITS = 1,          /* >0: cut every key range into this many chunks; 0 = cost model */
     FANOUT_OPT_VALIDATE_TABLE = 2,  /* 1: check page-table entries on the host each call */
     FANOUT_OPT_WAIT_LIMIT_NS = 3,   /* bound of every device-side wait (default 1e9 ns) */
     FANOUT_OPT_NUM_SMS = 4          /* >0: plan for this many SMs instead of the device's */
@@ -169,14 +175,21 @@ FANOUT_API int fanout_set_option(int32_t option, int64_t value);
 FANOUT_API int fanout_set_profile_events(fanout_event_t before, fanout_event_t after);
 
 /* Host-side description of the work plan fanout_attn would run for a problem
- * (no device access). Writes up to `cap` unit records of 8 int32 each:
- *   {kv_head, branch, tok_begin, n_tok, key_begin, key_end, pos_base, slot}
- * (see the split-KV kernel), and the counts. Returns FANOUT_OK or an error
- * code with the same validation as fanout_attn. */
+ * (no device access), planned for `num_sms` persistent CTAs (<= 0: 148).
+ * Writes up to `cap` unit records of 8 int32 each, grouped by CTA:
+ *   {kv_head, branch, tok_begin, n_tok, key_begin, key_end, pos_base, part}
+ * (the query rows of n_tok tokens x the G heads of kv_head against keys
+ * [key_begin, key_end) of the branch; token r is at position pos_base + r for
+ * causal masking; part >= 0 is the unit's partial block, -1 a direct write),
+ * and up to `cta_cap` entries of cta_first (CTA c runs units
+ * [cta_first[c], cta_first[c+1])). Any output pointer may be NULL with a zero
+ * capacity. Returns FANOUT_OK or an error code with the same validation as
+ * fanout_attn. */
 FANOUT_API int fanout_plan(const int32_t *suffix_lens, const int32_t *q_rows_per_branch,
                 int32_t num_branches, int32_t prefix_len, int32_t H_q, int32_t H_kv,
                 int32_t page_size, int32_t causal, int32_t num_sms, int32_t *units,
-                int32_t cap, int32_t *n_units, int32_t *n_slots, int32_t *tok_slots);
+                int32_t cap, int32_t *n_units, int32_t *cta_first, int32_t cta_cap,
+                int32_t *n_ctas, int32_t *n_parts);
 
 /* Launches one tiny kernel whose single thread waits on a barrier nothing ever
  * completes, bounded by `limit_ns`; returns FANOUT_ETIMEOUT when the bound

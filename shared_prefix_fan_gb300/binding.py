@@ -32,11 +32,12 @@ ABI = {
                                            _vp, _vp]),
     "fanout_lse_merge": (ctypes.c_int, [_vp, _vp, _i32, _i64, _i32, _vp, _i32, _vp, _vp]),
     "fanout_last_error": (ctypes.c_int, [_vp]),
+    "fanout_last_error_detail": (ctypes.c_int, [_vp, _i32p, _i32p]),
     "fanout_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "fanout_set_option": (ctypes.c_int, [_i32, _i64]),
     "fanout_set_profile_events": (ctypes.c_int, [_vp, _vp]),
     "fanout_plan": (ctypes.c_int, [_i32p, _i32p, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32p,
-                                   _i32, _i32p, _i32p, _i32p]),
+                                   _i32, _i32p, _i32p, _i32, _i32p, _i32p]),
     "fanout_selftest_wait_timeout": (ctypes.c_int, [_i64, _vp]),
     "fanout_release": (ctypes.c_int, []),
     "fanout_version": (ctypes.c_char_p, []),
@@ -104,21 +105,21 @@ def fork(prefix_pages, suffix_lens, page_size: int, free_pages, max_pages: int) 
 
 
 def plan(suffix_lens, q_rows, prefix_len: int, h_q: int, h_kv: int, page_size: int,
-         causal: bool, num_sms: int = 148) -> Tuple[np.ndarray, int, np.ndarray]:
-    """The work plan fanout_attn would run: (units [n, 8], n_slots, tok_slots [R])."""
+         causal: bool, num_sms: int = 148) -> Tuple[np.ndarray, np.ndarray, int]:
+    """The work plan fanout_attn would run: (units [n, 8], cta_first [n_cta+1], n_parts)."""
     sl, tq = _i32arr(suffix_lens), _i32arr(q_rows)
     lib = load()
-    n_units, n_slots = ctypes.c_int32(0), ctypes.c_int32(0)
-    tok = np.zeros(int(tq.sum()) + 1, dtype=np.int32)
-    _check(lib.fanout_plan(_ptr(sl), _ptr(tq), int(sl.shape[0]), int(prefix_len), int(h_q),
-                           int(h_kv), int(page_size), int(bool(causal)), int(num_sms), None, 0,
-                           ctypes.byref(n_units), ctypes.byref(n_slots), _ptr(tok)), "fanout_plan")
+    n_units, n_ctas, n_parts = ctypes.c_int32(0), ctypes.c_int32(0), ctypes.c_int32(0)
+    args = (_ptr(sl), _ptr(tq), int(sl.shape[0]), int(prefix_len), int(h_q), int(h_kv),
+            int(page_size), int(bool(causal)), int(num_sms))
+    _check(lib.fanout_plan(*args, None, 0, ctypes.byref(n_units), None, 0, ctypes.byref(n_ctas),
+                           ctypes.byref(n_parts)), "fanout_plan")
     units = np.zeros((max(n_units.value, 1), 8), dtype=np.int32)
-    _check(lib.fanout_plan(_ptr(sl), _ptr(tq), int(sl.shape[0]), int(prefix_len), int(h_q),
-                           int(h_kv), int(page_size), int(bool(causal)), int(num_sms),
-                           _ptr(units), int(units.shape[0]), ctypes.byref(n_units),
-                           ctypes.byref(n_slots), _ptr(tok)), "fanout_plan")
-    return units[:n_units.value], int(n_slots.value), tok[:-1]
+    cta = np.zeros(n_ctas.value + 1, dtype=np.int32)
+    _check(lib.fanout_plan(*args, _ptr(units), int(units.shape[0]), ctypes.byref(n_units),
+                           _ptr(cta), int(cta.shape[0]), ctypes.byref(n_ctas),
+                           ctypes.byref(n_parts)), "fanout_plan")
+    return units[:n_units.value], cta, int(n_parts.value)
 
 
 def set_option(option: int, value: int) -> None:
@@ -212,6 +213,14 @@ def lse_merge(part_o, part_ml, out=None, lse=None, out_dtype: str = "f32", strea
 
 def last_error(stream=None) -> int:
     return int(load().fanout_last_error(_stream_handle(stream)))
+
+
+def last_error_detail(stream=None) -> Tuple[int, int, int]:
+    """(status, wait site, CTA) of the device error word, then cleared."""
+    site, block = ctypes.c_int32(0), ctypes.c_int32(0)
+    rc = load().fanout_last_error_detail(_stream_handle(stream), ctypes.byref(site),
+                                         ctypes.byref(block))
+    return int(rc), int(site.value), int(block.value)
 
 
 def set_profile_events(before=None, after=None) -> None:

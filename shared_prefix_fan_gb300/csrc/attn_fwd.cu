@@ -1,0 +1,678 @@
+// attn_fwd.cu -- split-KV fan-out attention kernel for sm_103a (GB300).
+//
+// A persistent CTA (at most one per SM) runs the list of work units the
+// planner assigned to it, one after the other, with the K/V ring flowing
+// across unit boundaries. A unit (see Unit) is the query rows of up to
+// NQ*128/G tokens x the G query heads of one KV head -- G folded into the MMA
+// M dimension (ADR-0060, TL;DR and section 5.2) -- against one contiguous key
+// range of one branch's logical sequence, gathered page by page through the
+// branch's page table ("AHBM Agentic Runtime Architecture" section 3.1).
+// Keys are swept in 128-key tiles with the FlashAttention online softmax of
+// ADR-0060 section 3, in base 2 with scale*log2(e) folded:
+//   S = Q K_j^T ; raise the reference max m when needed ; P = 2^(S - m) ;
+//   l = l corr + rowsum P ; O = O corr + P V_j .
+// m is raised only when a tile's row max exceeds it by more than 2^8 (lazy
+// rescaling): P then stays <= 256, O and l stay consistent with m, and the
+// O rescale in TMEM is almost never needed. Causal tiles entirely in the
+// future are never produced (the planner trims each unit's key range),
+// boundary tiles are masked per row (ADR-0060 section 5.4). A unit covering
+// all keys of its rows writes out = O / l and lse = (m + log2 l) ln 2;
+// otherwise the partial (m, l, O) goes to the unit's partial block for the
+// log-sum-exp merge (ADR-0060 section 4).
+//
+// GB300 mapping. NQ query tiles of 128 rows per unit (NQ = 1 for short row
+// blocks such as decode, 2 for long ones):
+//   warp 0     TMA producer: the unit's Q tiles (3-D boxes over [R][H_q][d]),
+//              then K/V tiles page by page into a ring of 32 KB stages
+//              (128-byte swizzle); page ids prefetched 32 at a time.
+//   warp 1     TMEM owner + single-thread tcgen05 issuer:
+//              S = Q K^T with Q and K from shared memory (both K-major);
+//              O += P V with P from TMEM and V from shared memory (MN-major).
+//   warps 2..  one softmax warpgroup per query tile: thread i owns row i
+//              (TMEM lane i); reads S (tcgen05.ld), masks, exponentiates,
+//              writes P as bf16 back over the first 64 columns of its S
+//              (tcgen05.st), and runs the epilogue.
+// TMEM (512 columns): NQ = 2: S_0 = 0, S_1 = 128, O_0 = 256, O_1 = 384;
+//                     NQ = 1: S double-buffered at 0 / 128 by tile parity, O = 256.
+// Issue order of the MMA thread per K/V tile j:
+//   NQ = 2: S_0(j), P.V_1(j-1), S_1(j), P.V_0(j): while one softmax group
+//           works, the tensor core runs the other group's products;
+//   NQ = 1: S(j), P.V(j-1): S of the next tile overlaps the softmax.
+// Since tcgen05 operations of one thread execute in order, an S that reuses
+// the TMEM holding an earlier P is issued after the P.V that reads that P.
+// Every wait is bounded (mbar_wait); on expiry the CTA records
+// FANOUT_ETIMEOUT, drains its own in-flight copies and MMAs, frees TMEM and
+// returns.
+#include <cuda_bf16.h>
+
+#include "fanout_internal.h"
+#include "ptx_sm100.cuh"
+
+namespace fanout {
+namespace {
+
+constexpr int kTileBytes = kBN * kHD * 2;   // one K or V tile, bf16
+constexpr int kHalfBytes = kTileBytes / 2;  // 128 rows x 64 columns (128 B rows)
+constexpr int kQBytes = kBM * kHD * 2;
+constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold (base-2 units)
+constexpr int kErrTimeout = 5;        // FANOUT_ETIMEOUT
+
+template <int NQ>
+struct Cfg {
+    static constexpr int kStages = NQ == 1 ? 6 : 5;
+    static constexpr int kThreads = 64 + 128 * NQ;
+    static constexpr int kSmemQ = 0;
+    static constexpr int kSmemRing = kSmemQ + NQ * kQBytes;
+    static constexpr int kSmemBar = kSmemRing + kStages * kTileBytes;
+    // barriers: ring full/empty, Q full/free, aux, drain, then 4 per softmax group
+    static constexpr int BAR_FULL = 0;
+    static constexpr int BAR_EMPTY = kStages;
+    static constexpr int BAR_QFULL = 2 * kStages;
+    static constexpr int BAR_QFREE = BAR_QFULL + 1;
+    static constexpr int BAR_AUX = BAR_QFULL + 2;
+    static constexpr int BAR_DRAIN = BAR_QFULL + 3;
+    static constexpr int BAR_GROUP = BAR_QFULL + 4;  // + 5 x + {SFULL, PFULL, ODONE, OFREE, SFREE}
+    static constexpr int kNumBars = BAR_GROUP + 5 * NQ;
+    static constexpr int kSmemMisc = kSmemBar + kNumBars * 8;
+    static constexpr int kSmemTotal = kSmemMisc + 16;
+    static constexpr int kSmemAlloc = kSmemTotal + 1024;  // base aligned up to 1024 B
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr uint32_t kColO = 256;
+    static_assert(kSmemAlloc <= 232448, "shared memory per CTA");
+};
+
+enum { SFULL = 0, PFULL = 1, ODONE = 2, OFREE = 3, SFREE = 4 };
+
+constexpr uint32_t kIdescQK = ptx::idesc_bf16_f32(kBM, kBN, false, false);
+constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(kBM, kHD, false, true);
+
+// TMEM column of the S (and P) buffer group x uses for its t-th tile.
+template <int NQ>
+__device__ __forceinline__ uint32_t s_col(int x, uint32_t t) {
+    return NQ == 2 ? 128u * x : 128u * (t & 1u);
+}
+
+template <int NQ>
+struct Smem {
+    using C = Cfg<NQ>;
+    uint32_t base;  // shared-window address of the 1024-aligned base
+    uint8_t* ptr;   // generic pointer to the same place
+    __device__ uint32_t bar(int i) const { return base + C::kSmemBar + 8u * i; }
+    __device__ uint32_t gbar(int x, int which) const { return bar(C::BAR_GROUP + 5 * x + which); }
+    __device__ uint32_t* tmem_slot() const { return reinterpret_cast<uint32_t*>(ptr + C::kSmemMisc); }
+    __device__ volatile int* abort_flag() const {
+        return reinterpret_cast<volatile int*>(ptr + C::kSmemMisc + 4);
+    }
+};
+
+__device__ __forceinline__ void record_timeout(const SplitParams& p, volatile int* abort_flag,
+                                               int site) {
+    *abort_flag = 1;
+    if (atomicCAS(p.err, 0, kErrTimeout) == 0) {
+        p.err[1] = site;
+        p.err[2] = static_cast<int32_t>(blockIdx.x);
+    }
+}
+
+__device__ __forceinline__ int unit_tiles(const Unit& u) {
+    return (u.key_end - u.key_begin + kBN - 1) / kBN;
+}
+
+// Query tiles of a unit that hold at least one row.
+template <int NQ>
+__device__ __forceinline__ int unit_nq(const Unit& u, int tpt) {
+    return (NQ == 2 && u.n_tok > tpt) ? 2 : 1;
+}
+
+// ------------------------------------------------------------------ producer
+template <int NQ>
+__device__ void producer_warp(const SplitParams& p, const Smem<NQ>& sm, const CUtensorMap* tm_q,
+                              const CUtensorMap* tm_k, const CUtensorMap* tm_v) {
+    using C = Cfg<NQ>;
+    const int lane = threadIdx.x & 31;
+    const uint64_t lim = p.wait_limit_ns;
+    volatile int* abort = sm.abort_flag();
+    const int ps = p.page_size;
+    const int box_bytes = p.G * p.tpt * 128;  // one half of one query tile
+    uint32_t it = 0;            // ring position
+    uint32_t issued_mask = 0;   // stages ever loaded
+    uint32_t issued_par = 0;    // parity of the last phase loaded per stage
+    bool aux_pending = false;
+    uint32_t aux_phase = 0;
+    bool ok = true;
+    int k = 0;
+    for (int ui = p.cta_first[blockIdx.x]; ui < p.cta_first[blockIdx.x + 1] && ok; ++ui) {
+        const Unit u = p.units[ui];
+        const int n_tiles = unit_tiles(u);
+        if (n_tiles <= 0) continue;
+        const int nq = unit_nq<NQ>(u, p.tpt);
+        // Q tiles: the Q buffers are free once the previous unit's last S MMA completed.
+        if (k > 0) {
+            bool w = true;
+            if (lane == 0) w = ptx::mbar_wait(sm.bar(C::BAR_QFREE), (k - 1) & 1, lim, abort);
+            if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; if (lane == 0) record_timeout(p, abort, 1); break; }
+        }
+        if (lane == 0) {
+            const uint32_t qb = sm.bar(C::BAR_QFULL);
+            ptx::mbar_arrive_expect_tx(qb, static_cast<uint32_t>(2 * nq * box_bytes));
+            const int y = u.kv_head * p.G;
+            for (int x = 0; x < nq; ++x) {
+                const uint32_t dst = sm.base + C::kSmemQ + x * kQBytes;
+                const int z = u.tok_begin + x * p.tpt;
+                ptx::tma_load_3d(dst, tm_q, qb, 0, y, z);
+                ptx::tma_load_3d(dst + kHalfBytes, tm_q, qb, 64, y, z);
+            }
+        }
+        // Page ids of the unit, 32 per window (lane l holds page l of the window),
+        // loaded one window ahead so no tile waits on the page table.
+        const int32_t* prow = p.page_table + static_cast<int64_t>(u.branch) * p.max_pages +
+                              u.key_begin / ps;
+        const int n_pages_unit = (u.key_end - u.key_begin + ps - 1) / ps;
+        const int ppt = kBN / ps;  // pages per tile: 1, 2, 4 or 8 (divides 32)
+        auto load_window = [&](int w) -> int {
+            const int idx = w * 32 + lane;
+            return idx < n_pages_unit ? __ldg(prow + idx) : 0;
+        };
+        int win = 0;
+        int win_cur = load_window(0);
+        int win_nxt = load_window(1);
+        for (int j = 0; j < n_tiles && ok; ++j) {
+            const int kt = u.key_begin + j * kBN;
+            const int n_valid = min(kBN, u.key_end - kt);
+            const int n_pg = (n_valid + ps - 1) / ps;
+            const int rel = j * ppt;  // first page of the tile, relative to the unit
+            if ((rel >> 5) != win) {
+                win = rel >> 5;
+                win_cur = win_nxt;
+                win_nxt = load_window(win + 1);
+            }
+            const int pg_off = rel & 31;
+            for (int kv = 0; kv < 2 && ok; ++kv, ++it) {
+                const uint32_t stage = it % C::kStages;
+                const uint32_t par = (it / C::kStages) & 1u;
+                bool w = true;
+                if (lane == 0) w = ptx::mbar_wait(sm.bar(C::BAR_EMPTY + stage), par ^ 1u, lim, abort);
+                if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; if (lane == 0) record_timeout(p, abort, 2); break; }
+                const uint32_t dst = sm.base + C::kSmemRing + stage * kTileBytes;
+                const CUtensorMap* tm = kv == 0 ? tm_k : tm_v;
+                const bool partial = n_valid < kBN;
+                const uint32_t bar = partial ? sm.bar(C::BAR_AUX) : sm.bar(C::BAR_FULL + stage);
+                if (lane == 0) ptx::mbar_arrive_expect_tx(bar, static_cast<uint32_t>(n_pg * ps) * 256u);
+                for (int pg = 0; pg < n_pg; ++pg) {
+                    const int page = __shfl_sync(0xffffffffu, win_cur, pg_off + pg);
+                    if (lane == 0) {
+                        const int row = (page * p.H_kv + u.kv_head) * ps;
+                        const uint32_t off = static_cast<uint32_t>(pg * ps) * 128u;
+                        ptx::tma_load_2d(dst + off, tm, bar, 0, row);
+                        ptx::tma_load_2d(dst + kHalfBytes + off, tm, bar, 64, row);
+                    }
+                }
+                if (lane == 0) {
+                    issued_mask |= 1u << stage;
+                    issued_par = (issued_par & ~(1u << stage)) | (par << stage);
+                }
+                if (partial) {
+                    // Tail tile: wait for the pages, then zero every row past the
+                    // last valid key so no stale value reaches the MMAs.
+                    aux_pending = true;
+                    bool w2 = true;
+                    if (lane == 0) w2 = ptx::mbar_wait(sm.bar(C::BAR_AUX), aux_phase, lim, abort);
+                    if (!__shfl_sync(0xffffffffu, w2, 0)) { ok = false; if (lane == 0) record_timeout(p, abort, 3); break; }
+                    aux_pending = false;
+                    aux_phase ^= 1u;
+                    const int n_zero = (kBN - n_valid) * 16;  // 16-byte chunks, both halves
+                    for (int idx = lane; idx < n_zero; idx += 32) {
+                        const int r = n_valid + (idx >> 4);
+                        const int ch = idx & 15;
+                        const uint32_t a = dst + (ch >> 3) * kHalfBytes + r * 128 + (ch & 7) * 16;
+                        ptx::st_shared_v4(a, 0u, 0u, 0u, 0u);
+                    }
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(sm.bar(C::BAR_FULL + stage));
+                }
+            }
+        }
+        ++k;
+    }
+    if (!ok && lane == 0) {
+        // Drain: every copy this warp started must land before the CTA exits.
+        for (int s = 0; s < C::kStages; ++s)
+            if (issued_mask & (1u << s))
+                ptx::mbar_wait(sm.bar(C::BAR_FULL + s), (issued_par >> s) & 1u, lim, nullptr);
+        if (aux_pending) ptx::mbar_wait(sm.bar(C::BAR_AUX), aux_phase, lim, nullptr);
+    }
+}
+
+// ------------------------------------------------------------------ MMA issuer
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile_base, int kk) {
+    // K-major, 128-byte swizzle: 64-column halves 16 KB apart, 8-row groups 1 KB
+    // apart; a 16-element K step advances 32 bytes inside the swizzle atom.
+    return ptx::sdesc_sw128(tile_base + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
+}
+__device__ __forceinline__ uint64_t vmn_desc(uint32_t tile_base, int kk) {
+    // V as the B operand of P.V: MN-major (d contiguous), 128-byte swizzle.
+    // LBO = distance between 64-column halves, SBO = between 8-key groups;
+    // a 16-key K step advances 16 rows = 2 KB.
+    return ptx::sdesc_sw128(tile_base + kk * 2048, kHalfBytes, 1024);
+}
+
+template <int NQ>
+struct MmaState {
+    uint32_t it0 = 0;      // ring position of the unit's K_0 (K_j at it0+2j, V_j at it0+2j+1)
+    uint32_t jt[NQ] = {};  // tiles each softmax group processed before this unit
+    int kx[NQ] = {};       // units each softmax group processed before this unit
+};
+
+template <int NQ>
+__device__ __forceinline__ bool issue_s(const SplitParams& p, const Smem<NQ>& sm, uint32_t tmem,
+                                        const MmaState<NQ>& st, int x, int j, uint32_t kb) {
+    using C = Cfg<NQ>;
+    // (the TMEM this S overwrites held a P whose P.V was issued earlier)
+    ptx::tc_fence_after();
+    const uint32_t qb = sm.base + C::kSmemQ + x * kQBytes;
+    const uint32_t d = tmem + s_col<NQ>(x, st.jt[x] + j);
+#pragma unroll
+    for (int kk = 0; kk < kHD / 16; ++kk)
+        ptx::mma_bf16_ss(d, kmajor_desc(qb, kk), kmajor_desc(kb, kk), kIdescQK, kk > 0);
+    ptx::mma_commit(sm.gbar(x, SFULL));
+    return true;
+}
+
+template <int NQ>
+__device__ __forceinline__ bool issue_pv(const SplitParams& p, const Smem<NQ>& sm, uint32_t tmem,
+                                         const MmaState<NQ>& st, int x, int jj, uint32_t vb) {
+    using C = Cfg<NQ>;
+    const uint64_t lim = p.wait_limit_ns;
+    volatile int* abort = sm.abort_flag();
+    // P of tile jj written (and O rescaled) by softmax x; for the unit's first
+    // product, the previous unit's O of group x read out.
+    if (!ptx::mbar_wait(sm.gbar(x, PFULL), (st.jt[x] + jj) & 1u, lim, abort)) { record_timeout(p, abort, 14); return false; }
+    if (jj == 0 && st.kx[x] > 0 &&
+        !ptx::mbar_wait(sm.gbar(x, OFREE), (st.kx[x] - 1) & 1, lim, abort)) { record_timeout(p, abort, 15); return false; }
+    ptx::tc_fence_after();
+    const uint32_t a = tmem + s_col<NQ>(x, st.jt[x] + jj);  // P: 64 columns of bf16 pairs
+    const uint32_t d = tmem + C::kColO + 128u * x;
+#pragma unroll
+    for (int kk = 0; kk < kBN / 16; ++kk)
+        ptx::mma_bf16_ts(d, a + 8u * kk, vmn_desc(vb, kk), kIdescPV, (jj > 0 || kk > 0) ? 1u : 0u);
+    ptx::mma_commit(sm.gbar(x, ODONE));
+    return true;
+}
+
+template <int NQ>
+__device__ void mma_thread(const SplitParams& p, const Smem<NQ>& sm, uint32_t tmem) {
+    using C = Cfg<NQ>;
+    const uint64_t lim = p.wait_limit_ns;
+    volatile int* abort = sm.abort_flag();
+    MmaState<NQ> st;
+    bool ok = true;
+    bool issued_any = false;
+    int k = 0;
+    auto stage_of = [&](uint32_t pos) { return pos % C::kStages; };
+    auto wait_full = [&](uint32_t pos, int site) -> bool {
+        if (ptx::mbar_wait(sm.bar(C::BAR_FULL + stage_of(pos)), (pos / C::kStages) & 1u, lim, abort))
+            return true;
+        record_timeout(p, abort, site);
+        return false;
+    };
+    auto ring = [&](uint32_t pos) { return sm.base + C::kSmemRing + stage_of(pos) * kTileBytes; };
+    for (int ui = p.cta_first[blockIdx.x]; ui < p.cta_first[blockIdx.x + 1] && ok; ++ui) {
+        const Unit u = p.units[ui];
+        const int n = unit_tiles(u);
+        if (n <= 0) continue;
+        const int nq = unit_nq<NQ>(u, p.tpt);
+        if (!ptx::mbar_wait(sm.bar(C::BAR_QFULL), k & 1, lim, abort)) { ok = false; record_timeout(p, abort, 10); break; }
+        for (int j = 0; j <= n && ok; ++j) {
+            const uint32_t posK = st.it0 + 2u * j, posV = posK + 1u, posVp = posK - 1u;
+            if (NQ == 2 && nq == 2) {
+                // S_0(j), P.V_1(j-1), S_1(j), P.V_0(j)
+                if (j < n) {
+                    if (!(ok = wait_full(posK, 11))) break;
+                    issue_s<NQ>(p, sm, tmem, st, 0, j, ring(posK));
+                    issued_any = true;
+                }
+                if (j > 0) {
+                    if (!(ok = issue_pv<NQ>(p, sm, tmem, st, 1, j - 1, ring(posVp)))) break;
+                    ptx::mma_commit(sm.bar(C::BAR_EMPTY + stage_of(posVp)));
+                }
+                if (j < n) {
+                    issue_s<NQ>(p, sm, tmem, st, 1, j, ring(posK));
+                    ptx::mma_commit(sm.bar(C::BAR_EMPTY + stage_of(posK)));
+                    if (j == n - 1) ptx::mma_commit(sm.bar(C::BAR_QFREE));
+                    if (!(ok = wait_full(posV, 13))) break;
+                    if (!(ok = issue_pv<NQ>(p, sm, tmem, st, 0, j, ring(posV)))) break;
+                }
+            } else if (NQ == 2) {
+                // one query tile only: S_0(j), P.V_0(j)
+                if (j < n) {
+                    if (!(ok = wait_full(posK, 11))) break;
+                    issue_s<NQ>(p, sm, tmem, st, 0, j, ring(posK));
+                    issued_any = true;
+                    ptx::mma_commit(sm.bar(C::BAR_EMPTY + stage_of(posK)));
+                    if (j == n - 1) ptx::mma_commit(sm.bar(C::BAR_QFREE));
+                    if (!(ok = wait_full(posV, 13))) break;
+                    if (!(ok = issue_pv<NQ>(p, sm, tmem, st, 0, j, ring(posV)))) break;
+                    ptx::mma_commit(sm.bar(C::BAR_EMPTY + stage_of(posV)));
+                }
+            } else {
+                // NQ == 1, S double-buffered: S(j), P.V(j-1). S(t) waits until the
+                // softmax has read S(t-1), so S-full never runs two phases ahead.
+                if (j < n) {
+                    if (!(ok = wait_full(posK, 11))) break;
+                    const uint32_t t = st.jt[0] + j;
+                    if (t > 0 && !ptx::mbar_wait(sm.gbar(0, SFREE), (t - 1) & 1u, lim, abort)) {
+                        ok = false;
+                        record_timeout(p, abort, 12);
+                        break;
+                    }
+                    issue_s<NQ>(p, sm, tmem, st, 0, j, ring(posK));
+                    issued_any = true;
+                    ptx::mma_commit(sm.bar(C::BAR_EMPTY + stage_of(posK)));
+                    if (j == n - 1) ptx::mma_commit(sm.bar(C::BAR_QFREE));
+                }
+                if (j > 0) {
+                    if (!(ok = wait_full(posVp, 13))) break;
+                    if (!(ok = issue_pv<NQ>(p, sm, tmem, st, 0, j - 1, ring(posVp)))) break;
+                    ptx::mma_commit(sm.bar(C::BAR_EMPTY + stage_of(posVp)));
+                }
+            }
+        }
+        st.it0 += 2u * n;
+        for (int x = 0; x < nq; ++x) {
+            st.jt[x] += n;
+            ++st.kx[x];
+        }
+        ++k;
+    }
+    if (!ok && issued_any) {
+        ptx::mma_commit(sm.bar(C::BAR_DRAIN));
+        ptx::mbar_wait(sm.bar(C::BAR_DRAIN), 0, lim, nullptr);
+    }
+}
+
+// ------------------------------------------------------------------ softmax
+__device__ __forceinline__ float max8(const float (&a)[8]) {
+    return fmaxf(fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])),
+                 fmaxf(fmaxf(a[4], a[5]), fmaxf(a[6], a[7])));
+}
+__device__ __forceinline__ float sum8(const float (&a)[8]) {
+    return ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
+}
+
+// Group x owns query tile x of every unit (rows 128x .. 128x+127); thread i
+// owns row i of the tile (TMEM lane i). A warp whose 32 rows are all padding
+// follows the barrier protocol but skips the TMEM traffic and the math.
+template <int NQ>
+__device__ void softmax_group(const SplitParams& p, const Smem<NQ>& sm, uint32_t tmem, int x) {
+    using C = Cfg<NQ>;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int quarter = warp & 3;  // TMEM lane quarter this warp may access
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t colO = C::kColO + 128u * x;
+    const uint64_t lim = p.wait_limit_ns;
+    volatile int* abort = sm.abort_flag();
+    const float sl2 = p.scale_log2;
+    const int rows_per_part = kBM * NQ;
+    uint32_t jt = 0;
+    bool ok = true;
+    for (int ui = p.cta_first[blockIdx.x]; ui < p.cta_first[blockIdx.x + 1] && ok; ++ui) {
+        const Unit u = p.units[ui];
+        const int n_tiles = unit_tiles(u);
+        if (n_tiles <= 0 || x >= unit_nq<NQ>(u, p.tpt)) continue;
+        const int urow = kBM * x + row;  // row within the unit
+        const bool row_valid = urow < u.n_tok * p.G;
+        const bool active = __any_sync(0xffffffffu, row_valid);
+        const int tok = u.tok_begin + urow / p.G;
+        const int hq = u.kv_head * p.G + urow % p.G;
+        const int vis_end = row_valid ? min(u.key_end, u.pos_base + tok + 1) : 0;
+        float m_ref = -INFINITY, l_run = 0.f;
+        for (int j = 0; j < n_tiles; ++j, ++jt) {
+            const int kt = u.key_begin + j * kBN;
+            bool w = ptx::mbar_wait(sm.gbar(x, SFULL), jt & 1u, lim, abort);
+            if (!__all_sync(0xffffffffu, w)) { ok = false; record_timeout(p, abort, 20); break; }
+            ptx::tc_fence_after();
+            const uint32_t colS = s_col<NQ>(x, jt);
+            float corr = 1.f;
+            if (active) {
+                uint32_t s[kBN];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t (&chunk)[32] = *reinterpret_cast<uint32_t (*)[32]>(&s[32 * c]);
+                    ptx::tmem_ld32(lane_addr + colS + 32 * c, chunk);
+                }
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t (&chunk)[32] = *reinterpret_cast<uint32_t (*)[32]>(&s[32 * c]);
+                    if (c == 0) ptx::tmem_ld_wait(chunk); else ptx::reg_touch(chunk);
+                }
+                if (NQ == 1) {
+                    ptx::tc_fence_before();
+                    ptx::mbar_arrive(sm.gbar(x, SFREE));
+                }
+                const int lim_c = vis_end - kt;  // visible columns of this tile for this row
+                float mx[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) mx[q] = -INFINITY;
+                if (lim_c >= kBN) {
+#pragma unroll
+                    for (int c = 0; c < kBN; ++c) mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(s[c]));
+                } else {
+#pragma unroll
+                    for (int c = 0; c < kBN; ++c) {
+                        const float v = (c < lim_c) ? __uint_as_float(s[c]) : -INFINITY;
+                        s[c] = __float_as_uint(v);
+                        mx[c & 7] = fmaxf(mx[c & 7], v);
+                    }
+                }
+                const float mt = max8(mx) * sl2;  // scale > 0: max commutes with scaling
+                if (mt > m_ref + kRescaleLog2) {
+                    corr = (m_ref == -INFINITY) ? 0.f : ptx::ex2(m_ref - mt);
+                    m_ref = mt;
+                }
+                const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+                float sm8[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) sm8[q] = 0.f;
+#pragma unroll
+                for (int c = 0; c < kBN; ++c) {
+                    const float e = ptx::ex2(fmaf(__uint_as_float(s[c]), sl2, -m_use));
+                    s[c] = __float_as_uint(e);
+                    sm8[c & 7] += e;
+                }
+                l_run = l_run * corr + sum8(sm8);
+                // P as bf16 pairs over the first 64 columns of this S buffer
+#pragma unroll
+                for (int i = 0; i < 64; ++i)
+                    s[i] = ptx::pack_bf16x2(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1]));
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t (&chunk)[32] = *reinterpret_cast<uint32_t (*)[32]>(&s[32 * c]);
+                    ptx::tmem_st32(lane_addr + colS + 32 * c, chunk);
+                }
+                ptx::tmem_st_wait();
+            } else if (NQ == 1) {
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(sm.gbar(x, SFREE));
+            }
+            if (j > 0) {
+                // The previous P.V must be done before O is rescaled in place; waiting
+                // for it every tile also keeps P-full from running two phases ahead
+                // of the MMA thread (it is normally complete already).
+                w = ptx::mbar_wait(sm.gbar(x, ODONE), (jt - 1) & 1u, lim, abort);
+                if (!__all_sync(0xffffffffu, w)) { ok = false; record_timeout(p, abort, 21); break; }
+                ptx::tc_fence_after();
+            }
+            if (j > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
+                uint32_t r[32];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    ptx::tmem_ld32(lane_addr + colO + 32 * c, r);
+                    ptx::tmem_ld_wait(r);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * corr);
+                    ptx::tmem_st32(lane_addr + colO + 32 * c, r);
+                }
+                ptx::tmem_st_wait();
+            }
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(sm.gbar(x, PFULL));
+        }
+        if (!ok) break;
+        // Epilogue: the last P.V done -> this row of O to global memory.
+        bool w = ptx::mbar_wait(sm.gbar(x, ODONE), (jt - 1) & 1u, lim, abort);
+        if (!__all_sync(0xffffffffu, w)) { ok = false; record_timeout(p, abort, 22); break; }
+        ptx::tc_fence_after();
+        if (active) {
+            const int64_t orow = static_cast<int64_t>(tok) * p.H_q + hq;
+            const bool direct = u.part < 0;
+            const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t r[32];
+                ptx::tmem_ld32(lane_addr + colO + 32 * c, r);
+                ptx::tmem_ld_wait(r);
+                if (!row_valid) continue;
+                if (direct && p.out_bf16) {
+                    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) +
+                                                          orow * kHD + 32 * c);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        dst[i] = make_uint4(
+                            ptx::pack_bf16x2(__uint_as_float(r[8 * i + 0]) * inv_l,
+                                             __uint_as_float(r[8 * i + 1]) * inv_l),
+                            ptx::pack_bf16x2(__uint_as_float(r[8 * i + 2]) * inv_l,
+                                             __uint_as_float(r[8 * i + 3]) * inv_l),
+                            ptx::pack_bf16x2(__uint_as_float(r[8 * i + 4]) * inv_l,
+                                             __uint_as_float(r[8 * i + 5]) * inv_l),
+                            ptx::pack_bf16x2(__uint_as_float(r[8 * i + 6]) * inv_l,
+                                             __uint_as_float(r[8 * i + 7]) * inv_l));
+                } else {
+                    const float sc = direct ? inv_l : 1.f;
+                    float* base = direct ? static_cast<float*>(p.out) + orow * kHD
+                                         : p.part_o + (static_cast<int64_t>(u.part) * rows_per_part +
+                                                       urow) * kHD;
+                    float4* dst = reinterpret_cast<float4*>(base + 32 * c);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        dst[i] = make_float4(__uint_as_float(r[4 * i + 0]) * sc,
+                                             __uint_as_float(r[4 * i + 1]) * sc,
+                                             __uint_as_float(r[4 * i + 2]) * sc,
+                                             __uint_as_float(r[4 * i + 3]) * sc);
+                }
+            }
+            if (row_valid) {
+                if (direct) {
+                    if (p.lse) p.lse[orow] = (m_ref + __log2f(l_run)) * 0.69314718055994531f;
+                } else {
+                    p.part_ml[static_cast<int64_t>(u.part) * rows_per_part + urow] =
+                        make_float2(m_ref, l_run);
+                }
+            }
+        }
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(sm.gbar(x, OFREE));
+    }
+}
+
+template <int NQ>
+__global__ void __launch_bounds__(Cfg<NQ>::kThreads, 1) __maxnreg__(NQ == 2 ? 200 : 255)
+    attn_fwd_kernel(const __grid_constant__ SplitParams p,
+                    const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v) {
+    using C = Cfg<NQ>;
+    extern __shared__ uint8_t smem_raw[];
+    Smem<NQ> sm;
+    {
+        const uint32_t raw = ptx::smem_u32(smem_raw);
+        const uint32_t aligned = (raw + 1023u) & ~1023u;
+        sm.base = aligned;
+        sm.ptr = smem_raw + (aligned - raw);
+    }
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    // The dependent merge kernel may be scheduled now; it waits for this grid
+    // to complete before reading anything.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            ptx::mbar_init(sm.bar(C::BAR_FULL + s), 1);
+            ptx::mbar_init(sm.bar(C::BAR_EMPTY + s), 1);
+        }
+        ptx::mbar_init(sm.bar(C::BAR_QFULL), 1);
+        ptx::mbar_init(sm.bar(C::BAR_QFREE), 1);
+        ptx::mbar_init(sm.bar(C::BAR_AUX), 1);
+        ptx::mbar_init(sm.bar(C::BAR_DRAIN), 1);
+        for (int x = 0; x < NQ; ++x) {
+            ptx::mbar_init(sm.gbar(x, SFULL), 1);
+            ptx::mbar_init(sm.gbar(x, PFULL), 128);
+            ptx::mbar_init(sm.gbar(x, ODONE), 1);
+            ptx::mbar_init(sm.gbar(x, OFREE), 128);
+            ptx::mbar_init(sm.gbar(x, SFREE), 128);
+        }
+        *sm.abort_flag() = 0;
+        ptx::fence_barrier_init();
+        ptx::fence_proxy_async_smem();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tmap(&tm_q);
+        ptx::prefetch_tmap(&tm_k);
+        ptx::prefetch_tmap(&tm_v);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_u32(sm.tmem_slot()), C::kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *sm.tmem_slot();
+
+    if (warp == 0) {
+        producer_warp<NQ>(p, sm, &tm_q, &tm_k, &tm_v);
+    } else if (warp == 1) {
+        if (lane == 0) mma_thread<NQ>(p, sm, tmem);
+        __syncwarp();
+    } else {
+        softmax_group<NQ>(p, sm, tmem, (warp - 2) >> 2);
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+template <int NQ>
+cudaError_t launch_nq(const SplitParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                      const CUtensorMap& tm_v, int grid, cudaStream_t stream) {
+    static bool attr_set[64] = {};  // the attribute is set once per device
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+        e = cudaFuncSetAttribute(attn_fwd_kernel<NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Cfg<NQ>::kSmemAlloc);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) attr_set[dev] = true;
+    }
+    attn_fwd_kernel<NQ><<<grid, Cfg<NQ>::kThreads, Cfg<NQ>::kSmemAlloc, stream>>>(p, tm_q, tm_k,
+                                                                                 tm_v);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_split_attn(const SplitParams& p, const CUtensorMap& tm_q,
+                              const CUtensorMap& tm_k, const CUtensorMap& tm_v, int grid,
+                              cudaStream_t stream) {
+    return p.nq == 2 ? launch_nq<2>(p, tm_q, tm_k, tm_v, grid, stream)
+                     : launch_nq<1>(p, tm_q, tm_k, tm_v, grid, stream);
+}
+
+}  // namespace fanout

@@ -1,6 +1,7 @@
-// fanout_api.cu -- the C ABI (include/fanout.h): argument validation, the
-// page-table fork, work-plan caching, per-(device, stream) workspaces, TMA
-// tensor maps and kernel launches. No attention arithmetic happens here.
+// fanout_api.cu -- the C ABI (include/fanout.h): the page-table fork, options,
+// work-plan caching and the per-(device, stream) workspaces. The launch path
+// itself (checks, tensor maps, kernels) is in runtime.cpp. No attention
+// arithmetic happens here.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -33,12 +34,10 @@ struct Workspace {
     size_t cap = 0;
     std::vector<int32_t> key;  // plan cache key
     Plan plan;
-    size_t off_units = 0, off_tok = 0, off_ml = 0, off_o = 0;
+    Layout layout{};
     bool plan_ready = false;
 };
 std::map<std::pair<int, cudaStream_t>, Workspace*> g_ws;
-
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 int status_from_cuda(cudaError_t e) {
     if (e == cudaSuccess) return FANOUT_OK;
@@ -46,70 +45,7 @@ int status_from_cuda(cudaError_t e) {
     return FANOUT_ECUDA;
 }
 
-int get_encode() {
-    if (g_encode) return FANOUT_OK;
-    cudaDriverEntryPointQueryResult q;
-    void* fn = nullptr;
-    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
-                                                     cudaEnableDefault, &q);
-    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr) return FANOUT_ECUDA;
-    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    return FANOUT_OK;
-}
-
-size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
-
 bool ok_align16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-// Host-side checks shared by fanout_attn and fanout_plan.
-int validate_shape(const int32_t* suffix_lens, const int32_t* q_rows, int32_t B, int32_t P,
-                   int32_t H_q, int32_t H_kv, int32_t d, int32_t page_size, int32_t causal) {
-    if (B < 0 || P < 0 || H_q <= 0 || H_kv <= 0 || d <= 0 || page_size <= 0) return FANOUT_EINVAL;
-    if (B > 0 && (suffix_lens == nullptr || q_rows == nullptr)) return FANOUT_EINVAL;
-    if (H_q % H_kv != 0) return FANOUT_EINVAL;
-    if (d != kHD) return FANOUT_EUNSUPPORTED;
-    if (page_size != 16 && page_size != 32 && page_size != 64 && page_size != 128)
-        return FANOUT_EUNSUPPORTED;
-    if (H_q / H_kv > kBM) return FANOUT_EUNSUPPORTED;
-    if (P % page_size != 0) return FANOUT_EUNSUPPORTED;
-    int64_t R = 0;
-    for (int32_t b = 0; b < B; ++b) {
-        const int32_t S = suffix_lens[b], T = q_rows[b];
-        if (S < 0 || T < 0) return FANOUT_EINVAL;
-        if (static_cast<int64_t>(P) + S > (1 << 29)) return FANOUT_EUNSUPPORTED;
-        if (causal && T > S) return FANOUT_EINVAL;     // new tokens are the suffix tail
-        if (T > 0 && static_cast<int64_t>(P) + S == 0) return FANOUT_EINVAL;  // nothing to see
-        R += T;
-    }
-    if (R * H_q > (static_cast<int64_t>(1) << 31) / kHD) return FANOUT_EUNSUPPORTED;
-    return FANOUT_OK;
-}
-
-int encode_2d_pool(CUtensorMap* m, const void* base, int64_t rows, int32_t page_size) {
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHD), static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHD) * 2};
-    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(page_size)};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
-                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? FANOUT_OK : FANOUT_ECUDA;
-}
-
-int encode_q(CUtensorMap* m, const void* q, int64_t R, int32_t H_q, int32_t G, int32_t tpt) {
-    cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHD), static_cast<cuuint64_t>(H_q),
-                          static_cast<cuuint64_t>(R)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHD) * 2,
-                             static_cast<cuuint64_t>(H_q) * kHD * 2};
-    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(tpt)};
-    cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims,
-                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? FANOUT_OK : FANOUT_ECUDA;
-}
 
 int device_sms(int dev) {
     if (g_num_sms_override > 0) return static_cast<int>(g_num_sms_override);
@@ -119,6 +55,13 @@ int device_sms(int dev) {
 }
 
 }  // namespace
+
+namespace fanout {
+int32_t current_force_splits() {
+    std::lock_guard<std::mutex> lk(g_mu);
+    return static_cast<int32_t>(g_force_splits);
+}
+}  // namespace fanout
 
 extern "C" {
 
@@ -194,11 +137,13 @@ int fanout_set_profile_events(fanout_event_t before, fanout_event_t after) {
 int fanout_plan(const int32_t* suffix_lens, const int32_t* q_rows_per_branch,
                 int32_t num_branches, int32_t prefix_len, int32_t H_q, int32_t H_kv,
                 int32_t page_size, int32_t causal, int32_t num_sms, int32_t* units, int32_t cap,
-                int32_t* n_units, int32_t* n_slots, int32_t* tok_slots) {
+                int32_t* n_units, int32_t* cta_first, int32_t cta_cap, int32_t* n_ctas,
+                int32_t* n_parts) {
     int st = validate_shape(suffix_lens, q_rows_per_branch, num_branches, prefix_len, H_q, H_kv,
                             kHD, page_size, causal);
     if (st != FANOUT_OK) return st;
-    if (cap < 0 || (cap > 0 && !units)) return FANOUT_EINVAL;
+    if (cap < 0 || (cap > 0 && !units) || cta_cap < 0 || (cta_cap > 0 && !cta_first))
+        return FANOUT_EINVAL;
     PlanInput in{suffix_lens, q_rows_per_branch, num_branches, prefix_len, H_q, H_kv,
                  page_size, causal, num_sms > 0 ? num_sms : 148,
                  static_cast<int32_t>(g_force_splits)};
@@ -207,10 +152,12 @@ int fanout_plan(const int32_t* suffix_lens, const int32_t* q_rows_per_branch,
     if (st != FANOUT_OK) return st;
     const int32_t n = static_cast<int32_t>(plan.units.size());
     if (n_units) *n_units = n;
-    if (n_slots) *n_slots = plan.n_slots;
+    if (n_ctas) *n_ctas = plan.n_cta();
+    if (n_parts) *n_parts = plan.n_parts;
     for (int32_t i = 0; i < std::min(n, cap); ++i)
         std::memcpy(units + 8 * static_cast<int64_t>(i), &plan.units[i], sizeof(Unit));
-    if (tok_slots) std::copy(plan.tok_slots.begin(), plan.tok_slots.end(), tok_slots);
+    for (int32_t i = 0; i < std::min<int32_t>(static_cast<int32_t>(plan.cta_first.size()), cta_cap); ++i)
+        cta_first[i] = plan.cta_first[i];
     return FANOUT_OK;
 }
 
@@ -224,26 +171,19 @@ int fanout_attn(const void* q, const void* k_pages, const void* v_pages,
                             d, page_size, causal);
     if (st != FANOUT_OK) return st;
     if (out_dtype != FANOUT_OUT_F32 && out_dtype != FANOUT_OUT_BF16) return FANOUT_EINVAL;
-    if (!(scale == scale) || scale == 0.0f) return FANOUT_EINVAL;
+    if (!(scale > 0.0f) || scale > 3.0e38f) return FANOUT_EINVAL;  // positive, finite
     int64_t R = 0;
-    int64_t need_pages = 0;
-    for (int32_t b = 0; b < num_branches; ++b) {
-        R += q_rows_per_branch[b];
-        need_pages = std::max<int64_t>(
-            need_pages, (static_cast<int64_t>(prefix_len) + suffix_lens[b] + page_size - 1) / page_size);
-    }
+    for (int32_t b = 0; b < num_branches; ++b) R += q_rows_per_branch[b];
     if (R == 0) return FANOUT_OK;
-    if (!q || !k_pages || !v_pages || !page_table || !out) return FANOUT_EINVAL;
-    if (!ok_align16(q) || !ok_align16(k_pages) || !ok_align16(v_pages) || !ok_align16(out))
-        return FANOUT_EINVAL;
-    if (num_pages <= 0 || max_pages_per_branch < need_pages) return FANOUT_EINVAL;
+    st = validate_call(q, k_pages, v_pages, page_table, suffix_lens, num_branches, prefix_len,
+                       max_pages_per_branch, num_pages, page_size, scale, out_dtype, out);
+    if (st != FANOUT_OK) return st;
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
 
     std::lock_guard<std::mutex> lk(g_mu);
     int dev = 0;
     cudaError_t ce = cudaGetDevice(&dev);
     if (ce != cudaSuccess) return status_from_cuda(ce);
-    if ((st = get_encode()) != FANOUT_OK) return st;
 
     if (g_validate_table) {
         std::vector<int32_t> tab(static_cast<size_t>(num_branches) * max_pages_per_branch);
@@ -274,85 +214,30 @@ int fanout_attn(const void* q, const void* k_pages, const void* v_pages,
                      page_size, causal, sms, static_cast<int32_t>(g_force_splits)};
         ws->plan_ready = false;
         if ((st = build_plan(in, ws->plan)) != FANOUT_OK) return st;
-        const Plan& pl = ws->plan;
-        size_t off = 0;
-        ws->off_units = off;
-        off = align_up(off + pl.units.size() * sizeof(Unit), 256);
-        ws->off_tok = off;
-        off = align_up(off + pl.tok_slots.size() * sizeof(int32_t), 256);
-        ws->off_ml = off;
-        off = align_up(off + static_cast<size_t>(pl.n_slots) * R * H_q * sizeof(float2), 256);
-        ws->off_o = off;
-        off = align_up(off + static_cast<size_t>(pl.n_slots) * R * H_q * kHD * sizeof(float), 256);
-        if (off > ws->cap) {
+        ws->layout = plan_layout(ws->plan);
+        if (ws->layout.total > ws->cap) {
             if (ws->buf) {
                 cudaStreamSynchronize(stream);
                 cudaFree(ws->buf);
                 ws->buf = nullptr;
                 ws->cap = 0;
             }
-            ce = cudaMalloc(&ws->buf, off);
+            ce = cudaMalloc(&ws->buf, ws->layout.total);
             if (ce != cudaSuccess) {
                 ws->buf = nullptr;
                 return status_from_cuda(ce);
             }
-            ws->cap = off;
+            ws->cap = ws->layout.total;
         }
-        uint8_t* base = static_cast<uint8_t*>(ws->buf);
-        ce = cudaMemcpyAsync(base + ws->off_units, pl.units.data(), pl.units.size() * sizeof(Unit),
-                             cudaMemcpyHostToDevice, stream);
-        if (ce == cudaSuccess)
-            ce = cudaMemcpyAsync(base + ws->off_tok, pl.tok_slots.data(),
-                                 pl.tok_slots.size() * sizeof(int32_t), cudaMemcpyHostToDevice,
-                                 stream);
+        ce = upload_plan(ws->plan, ws->layout, static_cast<uint8_t*>(ws->buf), stream);
         if (ce != cudaSuccess) return status_from_cuda(ce);
         ws->key = key;
         ws->plan_ready = true;
     }
-    const Plan& pl = ws->plan;
-    uint8_t* base = static_cast<uint8_t*>(ws->buf);
-    const int32_t G = H_q / H_kv;
-
-    CUtensorMap tm_q, tm_k, tm_v;
-    const int64_t pool_rows = static_cast<int64_t>(num_pages) * H_kv * page_size;
-    if ((st = encode_q(&tm_q, q, R, H_q, G, pl.tpt)) != FANOUT_OK) return st;
-    if ((st = encode_2d_pool(&tm_k, k_pages, pool_rows, page_size)) != FANOUT_OK) return st;
-    if ((st = encode_2d_pool(&tm_v, v_pages, pool_rows, page_size)) != FANOUT_OK) return st;
-
-    int32_t* err = nullptr;
-    if ((ce = err_word_ptr(&err)) != cudaSuccess) return status_from_cuda(ce);
-
-    SplitParams p;
-    p.page_table = page_table;
-    p.units = reinterpret_cast<const Unit*>(base + ws->off_units);
-    p.part_o = reinterpret_cast<float*>(base + ws->off_o);
-    p.part_ml = reinterpret_cast<float2*>(base + ws->off_ml);
-    p.out = out;
-    p.lse = lse;
-    p.err = err;
-    p.n_units = static_cast<int32_t>(pl.units.size());
-    p.max_pages = max_pages_per_branch;
-    p.R = static_cast<int32_t>(R);
-    p.H_q = H_q;
-    p.H_kv = H_kv;
-    p.G = G;
-    p.page_size = page_size;
-    p.tpt = pl.tpt;
-    p.out_bf16 = out_dtype == FANOUT_OUT_BF16;
-    p.scale_log2 = scale * 1.4426950408889634f;
-    p.wait_limit_ns = g_wait_limit_ns;
-
-    if (g_ev_before) cudaEventRecord(g_ev_before, stream);
-    ce = launch_split_attn(p, tm_q, tm_k, tm_v, p.n_units, stream);
-    if (g_ev_after) cudaEventRecord(g_ev_after, stream);
-    if (ce != cudaSuccess) return status_from_cuda(ce);
-    if (pl.need_merge) {
-        ce = launch_lse_merge(p.part_o, p.part_ml,
-                              reinterpret_cast<const int32_t*>(base + ws->off_tok), pl.n_slots,
-                              R * H_q, H_q, out, p.out_bf16, lse, stream);
-        if (ce != cudaSuccess) return status_from_cuda(ce);
-    }
-    return FANOUT_OK;
+    CallArgs a{q, k_pages, v_pages, page_table, max_pages_per_branch, num_pages, H_q, H_kv,
+               page_size, out_dtype == FANOUT_OUT_BF16, scale, out, lse, R, g_wait_limit_ns};
+    return launch_plan(a, ws->plan, ws->layout, static_cast<uint8_t*>(ws->buf), stream,
+                       g_ev_before, g_ev_after);
 }
 
 int fanout_lse_merge(const float* part_o, const float* part_ml, int32_t n_parts, int64_t n_out,
@@ -365,13 +250,23 @@ int fanout_lse_merge(const float* part_o, const float* part_ml, int32_t n_parts,
     if (n_parts == 0 || !part_o || !part_ml || !out) return FANOUT_EINVAL;
     if (!ok_align16(part_o) || !ok_align16(out) || (reinterpret_cast<uintptr_t>(part_ml) & 7u))
         return FANOUT_EINVAL;
-    cudaError_t ce = launch_lse_merge(part_o, reinterpret_cast<const float2*>(part_ml), nullptr,
-                                      n_parts, n_out, 1, out, out_dtype == FANOUT_OUT_BF16, lse,
-                                      reinterpret_cast<cudaStream_t>(stream));
-    return status_from_cuda(ce);
+    MergeParams m;
+    m.part_o = part_o;
+    m.part_ml = reinterpret_cast<const float2*>(part_ml);
+    m.merge_ptr = nullptr;
+    m.merge_ent = nullptr;
+    m.n_parts = n_parts;
+    m.n_out = n_out;
+    m.H_q = 1;
+    m.G = 1;
+    m.rows_per_part = 0;
+    m.out = out;
+    m.out_bf16 = out_dtype == FANOUT_OUT_BF16;
+    m.lse = lse;
+    return status_from_cuda(launch_lse_merge(m, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-int fanout_last_error(fanout_stream_t stream) {
+int fanout_last_error_detail(fanout_stream_t stream, int32_t* site, int32_t* block) {
     cudaError_t ce = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
     if (ce != cudaSuccess) return status_from_cuda(ce);
     int32_t* err = nullptr;
@@ -379,12 +274,18 @@ int fanout_last_error(fanout_stream_t stream) {
     int32_t word[4] = {0, 0, 0, 0};
     ce = cudaMemcpy(word, err, sizeof(word), cudaMemcpyDeviceToHost);
     if (ce != cudaSuccess) return status_from_cuda(ce);
+    if (site) *site = word[1];
+    if (block) *block = word[2];
     if (word[0] != 0) {
         const int32_t zero[4] = {0, 0, 0, 0};
         cudaMemcpy(err, zero, sizeof(zero), cudaMemcpyHostToDevice);
         return word[0];
     }
     return FANOUT_OK;
+}
+
+int fanout_last_error(fanout_stream_t stream) {
+    return fanout_last_error_detail(stream, nullptr, nullptr);
 }
 
 int fanout_selftest_wait_timeout(int64_t limit_ns, fanout_stream_t stream) {

@@ -19,8 +19,9 @@ constexpr int kNoCausal = 1 << 30;  // pos_base for units that need no causal ma
 // [key_begin, key_end) of branch `branch`'s logical sequence.
 // Token r (global index) sits at absolute position pos_base + r, and key j
 // is visible to it iff j < key_end and j <= pos_base + r.
-// slot >= 0: write the unnormalised partial (m, l, o) into partial slot `slot`;
-// slot < 0: this unit covers every visible key of its rows, write final out/lse.
+// part >= 0: write the unnormalised partial (m, l, o) of the tile's rows into
+// partial block `part` (128 * nq rows); part < 0: this unit covers every visible key
+// of its rows, write the final out / lse.
 struct Unit {
     int32_t kv_head;
     int32_t branch;
@@ -29,7 +30,7 @@ struct Unit {
     int32_t key_begin;
     int32_t key_end;
     int32_t pos_base;
-    int32_t slot;
+    int32_t part;
 };
 static_assert(sizeof(Unit) == 32, "Unit is 8 int32");
 
@@ -40,17 +41,21 @@ struct PlanInput {
     int32_t prefix_len;
     int32_t H_q, H_kv, page_size;
     int32_t causal;
-    int32_t num_sms;
-    int32_t force_splits;
+    int32_t num_sms;       // persistent CTAs: at most one per SM
+    int32_t force_splits;  // >0: cut every key range into this many chunks
 };
 
 struct Plan {
-    std::vector<Unit> units;
-    std::vector<int32_t> tok_slots;  // per token: partial slots to merge (0 = written directly)
-    int32_t n_slots = 0;             // slots the partial buffer must hold
+    std::vector<Unit> units;         // grouped by CTA: CTA c runs units [cta_first[c], cta_first[c+1])
+    std::vector<int32_t> cta_first;  // n_cta + 1 entries
+    std::vector<int32_t> merge_ptr;  // R*H_kv + 1: partial entries of (token, KV head)
+    std::vector<int32_t> merge_ent;  // pairs {part, first row of the token in that unit's tile}
+    int32_t n_parts = 0;             // partial blocks of 128 * nq rows
     int32_t R = 0;
-    int32_t tpt = 0;                 // tokens per row tile
+    int32_t tpt = 0;                 // tokens per 128-row query tile
+    int32_t nq = 1;                  // query tiles per unit (1 or 2)
     bool need_merge = false;
+    int32_t n_cta() const { return cta_first.empty() ? 0 : static_cast<int32_t>(cta_first.size()) - 1; }
 };
 
 // Builds the work plan (host only). Returns a fanout_status code.
@@ -59,29 +64,75 @@ int build_plan(const PlanInput& in, Plan& plan);
 struct SplitParams {
     const int32_t* page_table;
     const Unit* units;
-    float* part_o;    // [slot][R*H_q][kHD]
-    float2* part_ml;  // [slot][R*H_q]   (m in log2 units, l)
+    const int32_t* cta_first;
+    float* part_o;    // [part][128 * nq rows][kHD]
+    float2* part_ml;  // [part][128 * nq rows]   (m in log2 units, l)
     void* out;        // [R][H_q][kHD] fp32 or bf16
     float* lse;       // [R][H_q] or null
     int32_t* err;     // device error word
-    int32_t n_units;
     int32_t max_pages;
     int32_t R, H_q, H_kv, G, page_size, tpt;
+    int32_t nq;        // query tiles per unit: selects the kernel instance
     int32_t out_bf16;
     float scale_log2;  // scale * log2(e)
     unsigned long long wait_limit_ns;
 };
 
+struct MergeParams {
+    const float* part_o;
+    const float2* part_ml;
+    const int32_t* merge_ptr;  // null: uniform parts (n_parts per output, part-major)
+    const int32_t* merge_ent;
+    int32_t n_parts;           // uniform mode only
+    int64_t n_out;             // rows of out: R*H_q (or n for uniform mode)
+    int32_t H_q, G;            // planned mode: out row n = token*H_q + kv_head*G + g
+    int32_t rows_per_part;     // planned mode: rows of one partial block
+    void* out;
+    int32_t out_bf16;
+    float* lse;
+};
+
+// One call: validated arguments (host) for the shared launch path.
+struct CallArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const int32_t* page_table;
+    int32_t max_pages, num_pages, H_q, H_kv, page_size;
+    int32_t out_bf16;
+    float scale;
+    void* out;
+    float* lse;
+    int64_t R;
+    unsigned long long wait_limit_ns;
+};
+
+// Device layout of a plan inside one scratch buffer.
+struct Layout {
+    size_t units, cta, mptr, ment, ml, o, total;
+};
+Layout plan_layout(const Plan& pl);
+// Copies the plan's tables into `base` (device) on `stream`.
+cudaError_t upload_plan(const Plan& pl, const Layout& L, uint8_t* base, cudaStream_t stream);
+// Tensor maps + split kernel (+ merge); events, when given, bracket the split kernel.
+int launch_plan(const CallArgs& a, const Plan& pl, const Layout& L, uint8_t* base,
+                cudaStream_t stream, cudaEvent_t ev_before, cudaEvent_t ev_after);
+// The FANOUT_OPT_SPLITS setting (0 = planner's choice).
+int32_t current_force_splits();
+// Host-side argument checks shared by the entry points (fanout_status code).
+int validate_shape(const int32_t* suffix_lens, const int32_t* q_rows, int32_t B, int32_t P,
+                   int32_t H_q, int32_t H_kv, int32_t d, int32_t page_size, int32_t causal);
+int validate_call(const void* q, const void* k, const void* v, const int32_t* page_table,
+                  const int32_t* suffix_lens, int32_t B, int32_t P, int32_t max_pages,
+                  int32_t num_pages, int32_t page_size, float scale, int32_t out_dtype,
+                  const void* out);
+
 // Launchers (defined in the .cu files); return cudaError_t.
 cudaError_t launch_split_attn(const SplitParams& p, const CUtensorMap& tm_q,
                               const CUtensorMap& tm_k, const CUtensorMap& tm_v, int grid,
                               cudaStream_t stream);
-cudaError_t launch_lse_merge(const float* part_o, const float2* part_ml,
-                             const int32_t* tok_slots, int32_t n_parts, int64_t n_out,
-                             int32_t group, void* out, int32_t out_bf16, float* lse,
-                             cudaStream_t stream);
+cudaError_t launch_lse_merge(const MergeParams& p, cudaStream_t stream);
 cudaError_t err_word_ptr(int32_t** ptr);
 cudaError_t launch_wait_selftest(int32_t* err, unsigned long long limit_ns, cudaStream_t stream);
-int split_attn_smem_bytes();
 
 }  // namespace fanout

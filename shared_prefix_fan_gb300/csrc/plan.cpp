@@ -1,9 +1,10 @@
-// plan.cpp -- host work planner: packed query rows, split-KV units, partial slots.
+// plan.cpp -- host work planner: packed query rows, split-KV units, their
+// assignment to persistent CTAs, and the merge index.
 //
 // Rows ("AHBM Agentic Runtime Architecture" section 3.2, "Sub-agent query
 // batching"; ADR-0060 TL;DR and section 5.2): per KV head, the query rows of a
-// run of consecutive tokens times that head's G query heads form one 128-row
-// tile (token-major, so a tile is 128/G tokens x G heads).
+// run of consecutive tokens times that head's G query heads form a unit of
+// one or two 128-row query tiles (token-major: 128/G tokens x G heads each).
 //
 // Keys ("AHBM Agentic Runtime Architecture" sections 3.1 and 3.3):
 //   * When at least two branches have new rows and the prefix is non-empty,
@@ -14,11 +15,23 @@
 //   * Otherwise every branch's tiles take its whole context [0, P + S_b).
 //   Causal: a tile's key range ends after the last key its last token sees;
 //   tiles entirely in the future are never produced (ADR-0060 section 5.4).
-// Split-KV (ADR-0060 section 4, FlashDecoding): each range is cut into chunks
-// of whole 128-key tiles so the grid has about two units per SM; a row's
-// chunks are its partial slots, merged later in ascending slot order.
+//
+// Split-KV (ADR-0060 section 4; "AHBM Agentic Runtime Architecture" 2.2/3.3):
+// each range is cut into chunks of whole 128-key tiles. The chunk size comes
+// from a small cost model -- the analogue of the pages' policy estimate
+// T_A vs T_B ("AHBM Agentic Runtime Architecture" section 4.5) on one GPU:
+//   time(C) = max over CTAs of sum(tiles + unit overhead)     (LPT assignment)
+//           + partial-merge traffic spread over the CTAs + merge launch,
+// evaluated for a ladder of chunk sizes C and for an exact-balance split
+// (contiguous per-CTA quotas of tiles, Stream-K style); smallest estimate wins.
+// Units are assigned to at most one persistent CTA per SM, longest first to
+// the least-loaded CTA. Among equal units the order is (key chunk, KV head,
+// row tile), so equal units land round-robin and the k-th units of all CTAs
+// read the same key chunk at about the same time (shared through L2).
 #include <algorithm>
 #include <cstdint>
+#include <functional>
+#include <queue>
 #include <tuple>
 #include <vector>
 
@@ -28,11 +41,122 @@ namespace fanout {
 namespace {
 
 struct Range {
-    int32_t branch, tok_begin, n_tok, lo, hi, pos_base;
-    bool prefix;
+    int32_t kv_head, branch, tok_begin, n_tok, lo, hi, pos_base;
+    bool complete;  // covers every visible key of its rows (no other range does)
 };
 
 inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+constexpr double kUnitOverhead = 2.0;  // prologue + epilogue of a unit, in tile times
+constexpr double kMergePerPart = 2.0;  // write + read of one 128-row partial, in tile times
+constexpr double kMergeLaunch = 4.0;   // the extra merge launch, in tile times
+
+struct Cand {
+    std::vector<Unit> units;   // in assignment order
+    std::vector<int64_t> work;
+    std::vector<int32_t> cta_of;
+    int32_t n_cta = 0;
+    double cost = 0;
+};
+
+// Cut the ranges with chunk size `chunk` tiles (0 = whole ranges), sort, assign.
+void make_candidate(const std::vector<Range>& ranges, int64_t chunk, int32_t force_splits,
+                    int32_t max_cta, Cand& c) {
+    struct Keyed {
+        int64_t work;
+        Unit u;
+        bool whole;
+    };
+    std::vector<Keyed> all;
+    for (const Range& r : ranges) {
+        const int64_t nkt = cdiv(r.hi - r.lo, kBN);
+        int64_t nch = force_splits > 0 ? force_splits : (chunk > 0 ? cdiv(nkt, chunk) : 1);
+        nch = std::max<int64_t>(1, std::min(nch, nkt));
+        for (int64_t ch = 0; ch < nch; ++ch) {
+            const int64_t t_lo = ch * nkt / nch, t_hi = (ch + 1) * nkt / nch;
+            const int32_t k_lo = r.lo + static_cast<int32_t>(t_lo) * kBN;
+            const int32_t k_hi = std::min<int32_t>(r.hi, r.lo + static_cast<int32_t>(t_hi) * kBN);
+            all.push_back({t_hi - t_lo,
+                           Unit{r.kv_head, r.branch, r.tok_begin, r.n_tok, k_lo, k_hi, r.pos_base,
+                                0},
+                           r.complete && nch == 1});
+        }
+    }
+    std::stable_sort(all.begin(), all.end(), [](const Keyed& a, const Keyed& b) {
+        return std::make_tuple(-a.work, a.u.key_begin, a.u.kv_head, a.u.branch, a.u.tok_begin) <
+               std::make_tuple(-b.work, b.u.key_begin, b.u.kv_head, b.u.branch, b.u.tok_begin);
+    });
+    c.n_cta = static_cast<int32_t>(std::min<int64_t>(max_cta, static_cast<int64_t>(all.size())));
+    c.units.clear();
+    c.work.clear();
+    c.cta_of.clear();
+    using Slot = std::pair<double, int32_t>;
+    std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
+    for (int32_t i = 0; i < c.n_cta; ++i) heap.push({0.0, i});
+    double makespan = 0;
+    int64_t n_parts = 0;
+    for (const Keyed& k : all) {
+        Slot s = heap.top();
+        heap.pop();
+        s.first += static_cast<double>(k.work) + kUnitOverhead;
+        makespan = std::max(makespan, s.first);
+        heap.push(s);
+        Unit u = k.u;
+        u.part = k.whole ? -1 : 0;  // partial indices are numbered later
+        if (!k.whole) ++n_parts;
+        c.units.push_back(u);
+        c.work.push_back(k.work);
+        c.cta_of.push_back(s.second);
+    }
+    c.cost = makespan + (n_parts > 0 ? kMergeLaunch + kMergePerPart * n_parts / c.n_cta : 0.0);
+}
+
+// Exact-balance candidate (Stream-K style): the ranges' tiles laid end to end
+// and cut into one contiguous quota per CTA; a CTA's quota may end inside a
+// range and the next CTA continues it.
+void make_streamk(const std::vector<Range>& ranges, int32_t max_cta, Cand& c) {
+    int64_t total = 0;
+    for (const Range& r : ranges) total += cdiv(r.hi - r.lo, kBN);
+    const int32_t n_cta = static_cast<int32_t>(std::min<int64_t>(max_cta, total));
+    // per-CTA quota in tile times, counting one unit overhead per range and per
+    // cut (about one cut per CTA)
+    const double quota = (static_cast<double>(total) +
+                          kUnitOverhead * static_cast<double>(ranges.size() + n_cta)) / n_cta;
+    c.units.clear();
+    c.work.clear();
+    c.cta_of.clear();
+    std::vector<double> load(n_cta, 0.0);
+    int32_t cta = 0;
+    int64_t n_parts = 0;
+    for (const Range& r : ranges) {
+        const int64_t nkt = cdiv(r.hi - r.lo, kBN);
+        int64_t t = 0;
+        while (t < nkt) {
+            const double room = quota - load[cta] - kUnitOverhead;
+            if (room < 0.5 && load[cta] > 0 && cta + 1 < n_cta) {
+                ++cta;
+                continue;
+            }
+            int64_t take = nkt - t;
+            if (cta + 1 < n_cta)
+                take = std::min<int64_t>(take, std::max<int64_t>(1, static_cast<int64_t>(room + 0.5)));
+            const int32_t k_lo = r.lo + static_cast<int32_t>(t) * kBN;
+            const int32_t k_hi = std::min<int32_t>(r.hi, r.lo + static_cast<int32_t>(t + take) * kBN);
+            const bool whole = r.complete && take == nkt;
+            c.units.push_back(Unit{r.kv_head, r.branch, r.tok_begin, r.n_tok, k_lo, k_hi, r.pos_base,
+                                   whole ? -1 : 0});
+            if (!whole) ++n_parts;
+            c.work.push_back(take);
+            c.cta_of.push_back(cta);
+            load[cta] += static_cast<double>(take) + kUnitOverhead;
+            t += take;
+        }
+    }
+    c.n_cta = cta + 1;
+    double makespan = 0;
+    for (double l : load) makespan = std::max(makespan, l);
+    c.cost = makespan + (n_parts > 0 ? kMergeLaunch + kMergePerPart * n_parts / c.n_cta : 0.0);
+}
 
 }  // namespace
 
@@ -41,97 +165,122 @@ int build_plan(const PlanInput& in, Plan& plan) {
     const int32_t B = in.num_branches;
     const int32_t P = in.prefix_len;
     const int32_t G = in.H_q / in.H_kv;
-    const int32_t tpt = kBM / G;
-    plan.tpt = tpt;
     std::vector<int32_t> tok0(B + 1, 0);
     int active = 0;
+    int32_t max_t = 0;
     for (int32_t b = 0; b < B; ++b) {
         tok0[b + 1] = tok0[b] + in.q_rows[b];
         if (in.q_rows[b] > 0) ++active;
+        max_t = std::max(max_t, in.q_rows[b]);
     }
     const int32_t R = tok0[B];
     plan.R = R;
-    plan.tok_slots.assign(R, 0);
     if (R == 0) return 0;
     const bool shared = active >= 2 && P > 0;
+    // Two 128-row query tiles per unit when the row blocks are long enough to
+    // fill them (they then share every K/V tile); one otherwise.
+    const int64_t block_rows = static_cast<int64_t>(shared ? R : max_t) * G;
+    plan.nq = block_rows > kBM ? 2 : 1;
+    plan.tpt = kBM / G;
+    const int32_t tpt = plan.tpt * plan.nq;  // tokens per unit
 
     std::vector<Range> ranges;
-    if (shared) {
-        for (int32_t t = 0; t < R; t += tpt)
-            ranges.push_back({0, t, std::min(tpt, R - t), 0, P, kNoCausal, true});
-    }
-    for (int32_t b = 0; b < B; ++b) {
-        const int32_t T = in.q_rows[b], S = in.suffix_lens[b];
-        for (int32_t t = tok0[b]; t < tok0[b + 1]; t += tpt) {
-            const int32_t n = std::min(tpt, tok0[b + 1] - t);
-            int32_t lo = shared ? P : 0;
-            int32_t hi = P + S;
-            int32_t pos_base = kNoCausal;
-            if (in.causal) {
-                pos_base = P + S - T - tok0[b];
-                hi = std::min(hi, pos_base + t + n);  // last token's pos + 1
+    for (int32_t h = 0; h < in.H_kv; ++h) {
+        if (shared) {
+            for (int32_t t = 0; t < R; t += tpt)
+                ranges.push_back({h, 0, t, std::min(tpt, R - t), 0, P, kNoCausal, false});
+        }
+        for (int32_t b = 0; b < B; ++b) {
+            const int32_t T = in.q_rows[b], S = in.suffix_lens[b];
+            for (int32_t t = tok0[b]; t < tok0[b + 1]; t += tpt) {
+                const int32_t n = std::min(tpt, tok0[b + 1] - t);
+                const int32_t lo = shared ? P : 0;
+                int32_t hi = P + S;
+                int32_t pos_base = kNoCausal;
+                if (in.causal) {
+                    pos_base = P + S - T - tok0[b];
+                    hi = std::min(hi, pos_base + t + n);  // last token's pos + 1
+                }
+                if (hi > lo) ranges.push_back({h, b, t, n, lo, hi, pos_base, !shared});
             }
-            if (hi > lo) ranges.push_back({b, t, n, lo, hi, pos_base, false});
         }
     }
 
-    // chunk size (in 128-key tiles) from the total work
-    int64_t work = 0;
-    for (const Range& r : ranges) work += cdiv(r.hi - r.lo, kBN);
-    work *= in.H_kv;
-    const int sms = std::max(1, in.num_sms);
-    const int64_t chunk = std::max<int64_t>(4, cdiv(work, 2LL * sms));
-    auto n_chunks = [&](const Range& r) -> int32_t {
-        const int64_t nkt = cdiv(r.hi - r.lo, kBN);
-        int64_t nch = in.force_splits > 0 ? in.force_splits : cdiv(nkt, chunk);
-        return static_cast<int32_t>(std::max<int64_t>(1, std::min(nch, nkt)));
-    };
+    // Chunk size from the cost model (or the forced split count).
+    const int32_t max_cta = std::max(1, in.num_sms);
+    Cand best, cand;
+    if (in.force_splits > 0) {
+        make_candidate(ranges, 0, in.force_splits, max_cta, best);
+    } else {
+        int64_t max_nkt = 1;
+        for (const Range& r : ranges) max_nkt = std::max(max_nkt, cdiv(r.hi - r.lo, kBN));
+        // keep the plan (and host planning time) bounded
+        const int64_t max_units =
+            std::max<int64_t>(16LL * max_cta, static_cast<int64_t>(ranges.size()));
+        bool first = true;
+        for (int64_t chunk : {0LL, 1024LL, 512LL, 384LL, 256LL, 192LL, 128LL, 96LL, 64LL, 48LL,
+                              32LL, 24LL, 16LL, 12LL, 8LL, 6LL, 4LL, 3LL, 2LL}) {
+            if (chunk > 0 && chunk >= max_nkt) continue;  // same as whole ranges
+            if (chunk > 0) {
+                int64_t n = 0;
+                for (const Range& r : ranges) n += cdiv(cdiv(r.hi - r.lo, kBN), chunk);
+                if (n > max_units) continue;
+            }
+            make_candidate(ranges, chunk, 0, max_cta, cand);
+            if (first || cand.cost < best.cost * 0.995) {
+                std::swap(best, cand);
+                first = false;
+            }
+        }
+        // Exact balance scatters CTAs over different key offsets; use it only
+        // when every KV byte fits in L2 several times over (the lockstep waves
+        // of the equal-chunk plan are what keeps a large shared prefix in L2).
+        int64_t kv_tokens = P;
+        for (int32_t b = 0; b < B; ++b) kv_tokens += in.suffix_lens[b];
+        const int64_t kv_bytes = kv_tokens * in.H_kv * kHD * 2 * 2;
+        if (kv_bytes <= (64LL << 20)) {
+            make_streamk(ranges, max_cta, cand);
+            if (cand.cost < best.cost * 0.97) std::swap(best, cand);
+        }
+    }
 
-    int32_t n_pre = 0;
-    if (shared) n_pre = n_chunks(ranges.front());
-    struct Keyed {
-        int64_t work;
-        int32_t chunk;
-        Unit u;
-    };
-    std::vector<Keyed> all;
-    for (const Range& r : ranges) {
-        const int32_t nch = n_chunks(r);
-        const int64_t nkt = cdiv(r.hi - r.lo, kBN);
-        const bool direct = !shared && nch == 1;
-        for (int32_t c = 0; c < nch; ++c) {
-            const int32_t t_lo = static_cast<int32_t>(c * nkt / nch);
-            const int32_t t_hi = static_cast<int32_t>((c + 1) * nkt / nch);
-            const int32_t k_lo = r.lo + t_lo * kBN;
-            const int32_t k_hi = std::min(r.hi, r.lo + t_hi * kBN);
-            int32_t slot = direct ? -1 : (r.prefix ? c : n_pre + c);
-            for (int32_t h = 0; h < in.H_kv; ++h)
-                all.push_back({t_hi - t_lo, c,
-                               Unit{h, r.branch, r.tok_begin, r.n_tok, k_lo, k_hi, r.pos_base,
-                                    slot}});
-        }
-        if (!r.prefix) {
-            const int32_t ns = direct ? 0 : n_pre + nch;
-            for (int32_t t = r.tok_begin; t < r.tok_begin + r.n_tok; ++t) plan.tok_slots[t] = ns;
-        }
+    // Group units by CTA (stable: each CTA keeps its assignment order) and
+    // number the partials in that order.
+    const int32_t n_cta = best.n_cta;
+    plan.cta_first.assign(n_cta + 1, 0);
+    for (int32_t c : best.cta_of) ++plan.cta_first[c + 1];
+    for (int32_t c = 0; c < n_cta; ++c) plan.cta_first[c + 1] += plan.cta_first[c];
+    std::vector<int32_t> fill(plan.cta_first.begin(), plan.cta_first.end() - 1);
+    plan.units.resize(best.units.size());
+    for (size_t i = 0; i < best.units.size(); ++i)
+        plan.units[fill[best.cta_of[i]]++] = best.units[i];
+    int32_t n_parts = 0;
+    for (Unit& u : plan.units)
+        if (u.part >= 0) u.part = n_parts++;
+    plan.n_parts = n_parts;
+
+    // Merge index: per (token, KV head), the partials covering it, in unit order.
+    if (n_parts > 0) {
+        std::vector<int32_t> count(static_cast<size_t>(R) * in.H_kv, 0);
+        for (const Unit& u : plan.units)
+            if (u.part >= 0)
+                for (int32_t t = u.tok_begin; t < u.tok_begin + u.n_tok; ++t)
+                    ++count[static_cast<size_t>(t) * in.H_kv + u.kv_head];
+        plan.merge_ptr.assign(count.size() + 1, 0);
+        for (size_t i = 0; i < count.size(); ++i) plan.merge_ptr[i + 1] = plan.merge_ptr[i] + count[i];
+        plan.merge_ent.resize(static_cast<size_t>(plan.merge_ptr.back()) * 2);
+        std::vector<int32_t> pos(plan.merge_ptr.begin(), plan.merge_ptr.end() - 1);
+        for (const Unit& u : plan.units)
+            if (u.part >= 0)
+                for (int32_t t = u.tok_begin; t < u.tok_begin + u.n_tok; ++t) {
+                    const size_t key = static_cast<size_t>(t) * in.H_kv + u.kv_head;
+                    const int32_t e = pos[key]++;
+                    plan.merge_ent[2 * e] = u.part;
+                    plan.merge_ent[2 * e + 1] = (t - u.tok_begin) * G;  // first row of t in u
+                }
+        // a (token, head) with a single direct unit has no entries: count 0
     }
-    if (shared) {
-        // tokens without a private range still merge their prefix chunks
-        for (int32_t t = 0; t < R; ++t)
-            if (plan.tok_slots[t] == 0) plan.tok_slots[t] = n_pre;
-    }
-    // Longest units first; among equals, units reading the same key chunk of
-    // the same KV head are adjacent so they run together and share it in L2.
-    std::stable_sort(all.begin(), all.end(), [](const Keyed& a, const Keyed& b) {
-        return std::make_tuple(-a.work, a.u.key_begin, a.u.kv_head, a.u.branch, a.u.tok_begin) <
-               std::make_tuple(-b.work, b.u.key_begin, b.u.kv_head, b.u.branch, b.u.tok_begin);
-    });
-    plan.units.reserve(all.size());
-    for (const Keyed& k : all) plan.units.push_back(k.u);
-    int32_t ns = 0;
-    for (int32_t t = 0; t < R; ++t) ns = std::max(ns, plan.tok_slots[t]);
-    plan.n_slots = ns;
-    plan.need_merge = ns > 0;
+    plan.need_merge = n_parts > 0;
     return 0;
 }
 

@@ -49,8 +49,8 @@ class DevWorkload:
                                 self.w.suffix_lens, self.w.q_rows, s.h_q, s.h_kv, s.page_size,
                                 s.scale, s.causal if causal is None else causal,
                                 out_dtype=out_dtype, stream=stream)
-        rc = binding.last_error(stream)
-        assert rc == binding.OK, f"device error {rc}: {binding.strerror(rc)}"
+        rc, site, block = binding.last_error_detail(stream)
+        assert rc == binding.OK, f"device error {rc}: {binding.strerror(rc)} (site {site}, block {block})"
         return out, lse
 
 

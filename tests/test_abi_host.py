@@ -74,6 +74,7 @@ def test_attn_rejects_bad_arguments_on_host(lib):
     assert _attn_rc(lib, maxp=2) == E          # table rows too narrow
     assert _attn_rc(lib, od=7) == E
     assert _attn_rc(lib, scale=0.0) == E
+    assert _attn_rc(lib, scale=-0.1) == E
     assert _attn_rc(lib, P=0, S=[0, 4], T=[1, 1], causal=0) == E  # a row with no key
     # nothing to do is not an error, and needs no device
     assert _attn_rc(lib, T=[0, 0], q=None, out=None) == binding.OK

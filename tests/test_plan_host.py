@@ -18,9 +18,15 @@ def _built():
 
 def check_plan(S, T, P, h_q, h_kv, ps, causal, sms=148):
     S, T = list(map(int, S)), list(map(int, T))
-    units, n_slots, tok_slots = binding.plan(S, T, P, h_q, h_kv, ps, causal, sms)
+    units, cta_first, n_parts = binding.plan(S, T, P, h_q, h_kv, ps, causal, sms)
     G = h_q // h_kv
     R = sum(T)
+    n_cta = len(cta_first) - 1
+    assert 1 <= n_cta <= max(1, sms)
+    assert cta_first[0] == 0 and cta_first[-1] == len(units)
+    assert (np.diff(cta_first) >= 1).all(), "a CTA without work"
+    parts = units[:, 7]
+    assert sorted(parts[parts >= 0].tolist()) == list(range(n_parts)), "partial blocks not 0..n-1"
     tok_branch = np.repeat(np.arange(len(T)), T)
     tok0 = np.concatenate([[0], np.cumsum(T)])
     vis = np.zeros(R, dtype=np.int64)
@@ -29,11 +35,11 @@ def check_plan(S, T, P, h_q, h_kv, ps, causal, sms=148):
         b = tok_branch[r]
         pos[r] = P + S[b] - T[b] + (r - tok0[b])
         vis[r] = min(P + S[b], pos[r] + 1) if causal else P + S[b]
-    covered = {}   # (r, h) -> list of (lo, hi, slot)
+    covered = {}   # (r, h) -> list of (lo, hi, part)
     total_pairs = 0
     for row in units:
-        h, br, tb, nt, k0, k1, pb, slot = (int(x) for x in row)
-        assert k1 > k0 >= 0 and nt >= 1 and nt * G <= 128 and 0 <= h < h_kv
+        h, br, tb, nt, k0, k1, pb, part = (int(x) for x in row)
+        assert k1 > k0 >= 0 and nt >= 1 and nt * G <= 256 and 0 <= h < h_kv  # one or two 128-row tiles
         assert k0 % ps == 0, "chunk start not page aligned"
         for r in range(tb, tb + nt):
             b = int(tok_branch[r])
@@ -44,7 +50,7 @@ def check_plan(S, T, P, h_q, h_kv, ps, causal, sms=148):
             else:
                 assert not causal or k1 <= P, "an unmasked unit reaches past the prefix"
             hi = min(k1, int(vis[r]))
-            covered.setdefault((r, h), []).append((k0, max(hi, k0), slot))
+            covered.setdefault((r, h), []).append((k0, max(hi, k0), part))
             total_pairs += max(0, hi - k0) * G
     for r in range(R):
         for h in range(h_kv):
@@ -56,14 +62,13 @@ def check_plan(S, T, P, h_q, h_kv, ps, causal, sms=148):
                 assert lo == cur or hi <= lo, (r, h, segs)
                 cur = max(cur, hi)
             assert cur == vis[r], (r, h, segs, vis[r])
-            slots = sorted(s for _, _, s in segs)
-            if tok_slots[r] == 0:
-                assert slots == [-1]
+            ps_ = [p_ for _, _, p_ in segs]
+            if -1 in ps_:
+                assert ps_ == [-1], "a direct unit shares its rows with another unit"
             else:
-                assert slots == list(range(tok_slots[r])), (r, slots, tok_slots[r])
-    assert n_slots == (max(tok_slots) if R else 0)
+                assert len(set(ps_)) == len(ps_)
     assert total_pairs == oracle.count_pairs(P, S, T, h_q, causal)
-    return units, n_slots, tok_slots
+    return units, cta_first, n_parts
 
 
 @pytest.mark.parametrize("name", ["tiny", "decode", "batching", "wide"])
@@ -75,19 +80,27 @@ def test_plan_workloads(name):
 
 def test_plan_prefill_is_direct():
     s = WORKLOADS["prefill"]
-    units, n_slots, tok_slots = binding.plan(s.suffix_lens, s.q_rows, s.prefix_len, s.h_q,
-                                             s.h_kv, s.page_size, s.causal, 148)
-    assert n_slots == 0 and (tok_slots == 0).all() and (units[:, 7] == -1).all()
-    assert len(units) == 8 * 8192 // 16
+    units, cta, n_parts = binding.plan(s.suffix_lens, s.q_rows, s.prefix_len, s.h_q,
+                                       s.h_kv, s.page_size, s.causal, 152)
+    assert n_parts == 0 and (units[:, 7] == -1).all()
+    # two 128-row query tiles per unit: 32 tokens x 8 heads
+    assert len(units) == 8 * 8192 // 32 and len(cta) == 153
 
 
-def test_plan_decode_split_32():
-    s = WORKLOADS["decode"]
-    units, n_slots, _ = binding.plan(s.suffix_lens, s.q_rows, s.prefix_len, s.h_q, s.h_kv,
-                                     s.page_size, s.causal, 152)
-    prefix_units = units[units[:, 5] <= s.prefix_len]
-    assert len(prefix_units) == 8 * 32   # 8 KV heads x 32 key splits of the shared prefix
-    assert n_slots == 33
+def _makespan(units, cta):
+    work = -(-(units[:, 5] - units[:, 4]) // 128) + 2
+    return max(work[cta[c]:cta[c + 1]].sum() for c in range(len(cta) - 1)), work.sum()
+
+
+@pytest.mark.parametrize("name", ["decode", "batching", "wide", "prefill"])
+def test_plan_balance(name):
+    """Persistent CTAs get nearly equal work (longest-first assignment)."""
+    w = draw(WORKLOADS[name])
+    s = w.spec
+    units, cta, _ = binding.plan(w.suffix_lens, w.q_rows, s.prefix_len, s.h_q, s.h_kv,
+                                 s.page_size, s.causal, 152)
+    mk, total = _makespan(units, cta)
+    assert mk <= 1.25 * total / (len(cta) - 1) + 40, (mk, total / (len(cta) - 1))
 
 
 @pytest.mark.parametrize("seed", range(12))
