@@ -379,9 +379,11 @@ __device__ void mma_thread(const SplitParams& p, const Smem<NQ>& sm, uint32_t tm
             }
         }
         st.it0 += 2u * n;
-        for (int x = 0; x < nq; ++x) {
-            st.jt[x] += n;
-            ++st.kx[x];
+        st.jt[0] += n;
+        ++st.kx[0];
+        if (NQ == 2 && nq == 2) {  // static indices keep the counters in registers
+            st.jt[NQ - 1] += n;
+            ++st.kx[NQ - 1];
         }
         ++k;
     }
@@ -434,37 +436,33 @@ __device__ void softmax_group(const SplitParams& p, const Smem<NQ>& sm, uint32_t
             bool w = ptx::mbar_wait(sm.gbar(x, SFULL), jt & 1u, lim, abort);
             if (!__all_sync(0xffffffffu, w)) { ok = false; record_timeout(p, abort, 20); break; }
             ptx::tc_fence_after();
+            if (NQ == 1) {
+                // S(jt) seen: the MMA may issue S(jt+1) into the other S buffer
+                // (its S-full then cannot run two phases ahead of this wait).
+                ptx::mbar_arrive(sm.gbar(x, SFREE));
+            }
             const uint32_t colS = s_col<NQ>(x, jt);
             float corr = 1.f;
             if (active) {
-                uint32_t s[kBN];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t (&chunk)[32] = *reinterpret_cast<uint32_t (*)[32]>(&s[32 * c]);
-                    ptx::tmem_ld32(lane_addr + colS + 32 * c, chunk);
-                }
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t (&chunk)[32] = *reinterpret_cast<uint32_t (*)[32]>(&s[32 * c]);
-                    if (c == 0) ptx::tmem_ld_wait(chunk); else ptx::reg_touch(chunk);
-                }
-                if (NQ == 1) {
-                    ptx::tc_fence_before();
-                    ptx::mbar_arrive(sm.gbar(x, SFREE));
-                }
                 const int lim_c = vis_end - kt;  // visible columns of this tile for this row
+                const bool full = lim_c >= kBN;
+                // Pass 1: the row max over the tile (two 32-column chunks per wait).
                 float mx[8];
 #pragma unroll
                 for (int q = 0; q < 8; ++q) mx[q] = -INFINITY;
-                if (lim_c >= kBN) {
 #pragma unroll
-                    for (int c = 0; c < kBN; ++c) mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(s[c]));
-                } else {
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t a[32], b[32];
+                    ptx::tmem_ld32(lane_addr + colS + 64 * h, a);
+                    ptx::tmem_ld32(lane_addr + colS + 64 * h + 32, b);
+                    ptx::tmem_ld_wait(a);
+                    ptx::reg_touch(b);
 #pragma unroll
-                    for (int c = 0; c < kBN; ++c) {
-                        const float v = (c < lim_c) ? __uint_as_float(s[c]) : -INFINITY;
-                        s[c] = __float_as_uint(v);
-                        mx[c & 7] = fmaxf(mx[c & 7], v);
+                    for (int i = 0; i < 32; ++i) {
+                        const int c0 = 64 * h + i, c1 = c0 + 32;
+                        const float v0 = (full || c0 < lim_c) ? __uint_as_float(a[i]) : -INFINITY;
+                        const float v1 = (full || c1 < lim_c) ? __uint_as_float(b[i]) : -INFINITY;
+                        mx[i & 7] = fmaxf(mx[i & 7], fmaxf(v0, v1));
                     }
                 }
                 const float mt = max8(mx) * sl2;  // scale > 0: max commutes with scaling
@@ -473,29 +471,35 @@ __device__ void softmax_group(const SplitParams& p, const Smem<NQ>& sm, uint32_t
                     m_ref = mt;
                 }
                 const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+                // Pass 2: P = 2^(S*scale*log2e - m), row sum, bf16 pairs written over
+                // S columns this pass has already read (chunk pair h -> P columns 32h..).
                 float sm8[8];
 #pragma unroll
                 for (int q = 0; q < 8; ++q) sm8[q] = 0.f;
 #pragma unroll
-                for (int c = 0; c < kBN; ++c) {
-                    const float e = ptx::ex2(fmaf(__uint_as_float(s[c]), sl2, -m_use));
-                    s[c] = __float_as_uint(e);
-                    sm8[c & 7] += e;
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int part = 0; part < 2; ++part) {
+                        uint32_t a[32];
+                        ptx::tmem_ld32(lane_addr + colS + 64 * h + 32 * part, a);
+                        ptx::tmem_ld_wait(a);
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2) {
+                            const int c = 64 * h + 32 * part + i;
+                            const float x0 = (full || c < lim_c) ? __uint_as_float(a[i]) : -INFINITY;
+                            const float x1 = (full || c + 1 < lim_c) ? __uint_as_float(a[i + 1]) : -INFINITY;
+                            const float e0 = ptx::ex2(fmaf(x0, sl2, -m_use));
+                            const float e1 = ptx::ex2(fmaf(x1, sl2, -m_use));
+                            sm8[i & 7] += e0;
+                            sm8[(i + 1) & 7] += e1;
+                            pk[16 * part + (i >> 1)] = ptx::pack_bf16x2(e0, e1);
+                        }
+                    }
+                    ptx::tmem_st32(lane_addr + colS + 32 * h, pk);
                 }
                 l_run = l_run * corr + sum8(sm8);
-                // P as bf16 pairs over the first 64 columns of this S buffer
-#pragma unroll
-                for (int i = 0; i < 64; ++i)
-                    s[i] = ptx::pack_bf16x2(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1]));
-#pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    uint32_t (&chunk)[32] = *reinterpret_cast<uint32_t (*)[32]>(&s[32 * c]);
-                    ptx::tmem_st32(lane_addr + colS + 32 * c, chunk);
-                }
                 ptx::tmem_st_wait();
-            } else if (NQ == 1) {
-                ptx::tc_fence_before();
-                ptx::mbar_arrive(sm.gbar(x, SFREE));
             }
             if (j > 0) {
                 // The previous P.V must be done before O is rescaled in place; waiting

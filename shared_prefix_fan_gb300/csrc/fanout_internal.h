@@ -48,8 +48,9 @@ struct PlanInput {
 struct Plan {
     std::vector<Unit> units;         // grouped by CTA: CTA c runs units [cta_first[c], cta_first[c+1])
     std::vector<int32_t> cta_first;  // n_cta + 1 entries
-    std::vector<int32_t> merge_ptr;  // R*H_kv + 1: partial entries of (token, KV head)
-    std::vector<int32_t> merge_ent;  // pairs {part, first row of the token in that unit's tile}
+    std::vector<int32_t> merge_cnt;  // R*H_kv: partial entries of (token, KV head)
+    std::vector<int32_t> merge_ent;  // [R*H_kv][merge_stride] pairs {part, first row of the token}
+    int32_t merge_stride = 0;
     int32_t n_parts = 0;             // partial blocks of 128 * nq rows
     int32_t R = 0;
     int32_t tpt = 0;                 // tokens per 128-row query tile
@@ -81,8 +82,9 @@ struct SplitParams {
 struct MergeParams {
     const float* part_o;
     const float2* part_ml;
-    const int32_t* merge_ptr;  // null: uniform parts (n_parts per output, part-major)
-    const int32_t* merge_ent;
+    const int32_t* merge_cnt;  // null: uniform parts (n_parts per output, part-major)
+    const int2* merge_ent;     // [key][stride] {part, row base}
+    int32_t merge_stride;
     int32_t n_parts;           // uniform mode only
     int64_t n_out;             // rows of out: R*H_q (or n for uniform mode)
     int32_t H_q, G;            // planned mode: out row n = token*H_q + kv_head*G + g
@@ -109,7 +111,7 @@ struct CallArgs {
 
 // Device layout of a plan inside one scratch buffer.
 struct Layout {
-    size_t units, cta, mptr, ment, ml, o, total;
+    size_t units, cta, mcnt, ment, ml, o, total;
 };
 Layout plan_layout(const Plan& pl);
 // Copies the plan's tables into `base` (device) on `stream`.

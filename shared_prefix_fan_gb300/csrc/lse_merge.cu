@@ -14,6 +14,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "fanout_internal.h"
 #include "ptx_sm100.cuh"
@@ -26,53 +27,59 @@ __device__ int32_t g_err_word[4];
 namespace {
 
 // One warp per output row n (a (token, query head) pair). Its partials are
-// either listed in the merge index (planned mode: entries {part, row base} of
-// the row's KV head, row = base + g) or uniform (part-major [n_parts][n_out]).
-// Up to 16 partials per pass: lane e loads entry e's (m, l) while every lane
-// loads its 4 columns of all 16 O vectors, so a row costs one memory round
-// trip; the weights are then formed with warp shuffles.
-constexpr int kMergeBatch = 16;
+// either listed in the merge index (planned mode: fixed-stride entry lists
+// {part, row base} per (token, KV head), row = base + g) or uniform
+// (part-major [n_parts][n_out]). The count and the first 32 entries of a row
+// load together; then up to kMergeBatch partials per pass: lane e loads entry
+// e's (m, l) while every lane loads its 4 columns of all the pass's O vectors,
+// so a row of up to kMergeBatch partials costs two memory round trips.
+constexpr int kMergeBatch = 24;
 
-__global__ void __launch_bounds__(256, 2) lse_merge_kernel(const MergeParams p) {
+__global__ void __launch_bounds__(256, 1) lse_merge_kernel(const MergeParams p) {
     // Launched as a programmatic dependent of the attention kernel: wait until
     // that grid has completed and its writes are visible.
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int lane = threadIdx.x & 31;
     const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
-    const int H_kv = p.merge_ptr ? p.H_q / p.G : 1;
+    const bool planned = p.merge_cnt != nullptr;
+    const int H_kv = planned ? p.H_q / p.G : 1;
     for (int64_t n = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
          n < p.n_out; n += warps) {
-        int32_t e0 = 0, ne = p.n_parts, g = 0;
-        if (p.merge_ptr) {
+        int32_t ne = p.n_parts, g = 0;
+        int64_t key = 0;
+        int2 ent0 = make_int2(0, 0);
+        if (planned) {
             const int64_t tok = n / p.H_q;
             const int32_t hq = static_cast<int32_t>(n % p.H_q);
-            const int64_t key = tok * H_kv + hq / p.G;
+            key = tok * H_kv + hq / p.G;
             g = hq % p.G;
-            e0 = p.merge_ptr[key];
-            ne = p.merge_ptr[key + 1] - e0;
+            if (lane < p.merge_stride) ent0 = p.merge_ent[key * p.merge_stride + lane];
+            ne = p.merge_cnt[key];
             if (ne <= 0) continue;  // written directly by the attention kernel
         }
-        auto row_of = [&](int32_t e) -> int64_t {
-            if (p.merge_ptr) {
-                const int32_t part = p.merge_ent[2 * (e0 + e)];
-                return static_cast<int64_t>(part) * p.rows_per_part + p.merge_ent[2 * (e0 + e) + 1] + g;
-            }
-            return static_cast<int64_t>(e) * p.n_out + n;
-        };
         float M = -INFINITY, L = 0.f;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int32_t c0 = 0; c0 < ne; c0 += kMergeBatch) {
             const int32_t cnt = min(kMergeBatch, ne - c0);
-            const int64_t my_row = (lane < cnt) ? row_of(c0 + lane) : 0;
+            int64_t my_row = 0;
+            if (lane < cnt) {
+                if (planned) {
+                    const int2 en = (c0 == 0) ? ent0 : p.merge_ent[key * p.merge_stride + c0 + lane];
+                    my_row = static_cast<int64_t>(en.x) * p.rows_per_part + en.y + g;
+                } else {
+                    my_row = static_cast<int64_t>(c0 + lane) * p.n_out + n;
+                }
+            }
             float2 ml = make_float2(-INFINITY, 0.f);
             if (lane < cnt) ml = p.part_ml[my_row];
             float4 o[kMergeBatch];
 #pragma unroll
             for (int u = 0; u < kMergeBatch; ++u) {
                 const int64_t r = __shfl_sync(0xffffffffu, my_row, min(u, cnt - 1));
-                o[u] = reinterpret_cast<const float4*>(p.part_o + r * kHD)[lane];
+                o[u] = (u < cnt) ? reinterpret_cast<const float4*>(p.part_o + r * kHD)[lane]
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
             }
-            // running (max, sum) over batches, in the base-2 domain
+            // running (max, sum) over passes, in the base-2 domain
             float mb = (ml.y > 0.f) ? ml.x : -INFINITY;
 #pragma unroll
             for (int s = 16; s > 0; s >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, s));
@@ -149,8 +156,19 @@ cudaError_t launch_lse_merge(const MergeParams& p, cudaStream_t stream) {
 
 // Device address of this device's error word (the symbol's host-side name is
 // only a stand-in; the address must come from the runtime, per device).
+// Looked up once per device (with that device current) and cached.
 cudaError_t err_word_ptr(int32_t** ptr) {
-    return cudaGetSymbolAddress(reinterpret_cast<void**>(ptr), g_err_word);
+    static int32_t* cached[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64 && cached[dev]) {
+        *ptr = cached[dev];
+        return cudaSuccess;
+    }
+    e = cudaGetSymbolAddress(reinterpret_cast<void**>(ptr), g_err_word);
+    if (e == cudaSuccess && dev >= 0 && dev < 64) cached[dev] = *ptr;
+    return e;
 }
 
 cudaError_t launch_wait_selftest(int32_t* err, unsigned long long limit_ns, cudaStream_t stream) {

@@ -233,12 +233,12 @@ int build_plan(const PlanInput& in, Plan& plan) {
             }
         }
         // Exact balance scatters CTAs over different key offsets; use it only
-        // when every KV byte fits in L2 several times over (the lockstep waves
-        // of the equal-chunk plan are what keeps a large shared prefix in L2).
+        // when the whole KV fits in L2 (otherwise the lockstep waves of the
+        // equal-chunk plan are what keeps a large shared prefix in L2).
         int64_t kv_tokens = P;
         for (int32_t b = 0; b < B; ++b) kv_tokens += in.suffix_lens[b];
         const int64_t kv_bytes = kv_tokens * in.H_kv * kHD * 2 * 2;
-        if (kv_bytes <= (64LL << 20)) {
+        if (kv_bytes <= (100LL << 20)) {
             make_streamk(ranges, max_cta, cand);
             if (cand.cost < best.cost * 0.97) std::swap(best, cand);
         }
@@ -259,26 +259,29 @@ int build_plan(const PlanInput& in, Plan& plan) {
         if (u.part >= 0) u.part = n_parts++;
     plan.n_parts = n_parts;
 
-    // Merge index: per (token, KV head), the partials covering it, in unit order.
+    // Merge index: per (token, KV head), the partials covering it, in unit order,
+    // as fixed-stride lists so a reader gets the count and the entries at once.
     if (n_parts > 0) {
-        std::vector<int32_t> count(static_cast<size_t>(R) * in.H_kv, 0);
+        const size_t n_keys = static_cast<size_t>(R) * in.H_kv;
+        plan.merge_cnt.assign(n_keys, 0);
         for (const Unit& u : plan.units)
             if (u.part >= 0)
                 for (int32_t t = u.tok_begin; t < u.tok_begin + u.n_tok; ++t)
-                    ++count[static_cast<size_t>(t) * in.H_kv + u.kv_head];
-        plan.merge_ptr.assign(count.size() + 1, 0);
-        for (size_t i = 0; i < count.size(); ++i) plan.merge_ptr[i + 1] = plan.merge_ptr[i] + count[i];
-        plan.merge_ent.resize(static_cast<size_t>(plan.merge_ptr.back()) * 2);
-        std::vector<int32_t> pos(plan.merge_ptr.begin(), plan.merge_ptr.end() - 1);
+                    ++plan.merge_cnt[static_cast<size_t>(t) * in.H_kv + u.kv_head];
+        int32_t stride = 1;
+        for (int32_t c : plan.merge_cnt) stride = std::max(stride, c);
+        plan.merge_stride = stride;
+        plan.merge_ent.assign(n_keys * stride * 2, 0);
+        std::vector<int32_t> fill_e(n_keys, 0);
         for (const Unit& u : plan.units)
             if (u.part >= 0)
                 for (int32_t t = u.tok_begin; t < u.tok_begin + u.n_tok; ++t) {
                     const size_t key = static_cast<size_t>(t) * in.H_kv + u.kv_head;
-                    const int32_t e = pos[key]++;
+                    const size_t e = key * stride + fill_e[key]++;
                     plan.merge_ent[2 * e] = u.part;
                     plan.merge_ent[2 * e + 1] = (t - u.tok_begin) * G;  // first row of t in u
                 }
-        // a (token, head) with a single direct unit has no entries: count 0
+        // a (token, head) covered by a single direct unit has count 0
     }
     plan.need_merge = n_parts > 0;
     return 0;

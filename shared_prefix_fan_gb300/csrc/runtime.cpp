@@ -116,8 +116,8 @@ Layout plan_layout(const Plan& pl) {
     off = align256(off + pl.units.size() * sizeof(Unit));
     L.cta = off;
     off = align256(off + pl.cta_first.size() * sizeof(int32_t));
-    L.mptr = off;
-    off = align256(off + pl.merge_ptr.size() * sizeof(int32_t));
+    L.mcnt = off;
+    off = align256(off + pl.merge_cnt.size() * sizeof(int32_t));
     L.ment = off;
     off = align256(off + pl.merge_ent.size() * sizeof(int32_t));
     L.ml = off;
@@ -135,9 +135,9 @@ cudaError_t upload_plan(const Plan& pl, const Layout& L, uint8_t* base, cudaStre
     if (e == cudaSuccess)
         e = cudaMemcpyAsync(base + L.cta, pl.cta_first.data(),
                             pl.cta_first.size() * sizeof(int32_t), cudaMemcpyHostToDevice, stream);
-    if (e == cudaSuccess && !pl.merge_ptr.empty())
-        e = cudaMemcpyAsync(base + L.mptr, pl.merge_ptr.data(),
-                            pl.merge_ptr.size() * sizeof(int32_t), cudaMemcpyHostToDevice, stream);
+    if (e == cudaSuccess && !pl.merge_cnt.empty())
+        e = cudaMemcpyAsync(base + L.mcnt, pl.merge_cnt.data(),
+                            pl.merge_cnt.size() * sizeof(int32_t), cudaMemcpyHostToDevice, stream);
     if (e == cudaSuccess && !pl.merge_ent.empty())
         e = cudaMemcpyAsync(base + L.ment, pl.merge_ent.data(),
                             pl.merge_ent.size() * sizeof(int32_t), cudaMemcpyHostToDevice, stream);
@@ -187,8 +187,9 @@ int launch_plan(const CallArgs& a, const Plan& pl, const Layout& L, uint8_t* bas
         MergeParams m;
         m.part_o = p.part_o;
         m.part_ml = p.part_ml;
-        m.merge_ptr = reinterpret_cast<const int32_t*>(base + L.mptr);
-        m.merge_ent = reinterpret_cast<const int32_t*>(base + L.ment);
+        m.merge_cnt = reinterpret_cast<const int32_t*>(base + L.mcnt);
+        m.merge_ent = reinterpret_cast<const int2*>(base + L.ment);
+        m.merge_stride = pl.merge_stride;
         m.n_parts = 0;
         m.n_out = a.R * a.H_q;
         m.H_q = a.H_q;
