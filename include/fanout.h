@@ -84,6 +84,46 @@ FANOUT_API int fanout_fork(const int32_t *prefix_pages, int32_t n_prefix_pages, 
                 int32_t n_free, int32_t *page_table, int32_t max_pages_per_branch);
 
 /*
+ * fanout_extend -- grow branch page tables for new tokens (host only).
+ * "AHBM Agentic Runtime Architecture" section 3.1 (private suffix pages per
+ * branch); ADR-0060 section 0.5.1 precondition P3 (the cache grows before
+ * attention). Branch b's private suffix grows from suffix_lens[b] to
+ * suffix_lens[b] + add_lens[b] tokens; the pages it now needs beyond its
+ * current ceil(suffix_lens[b] / page_size) are taken from free_pages in order
+ * (branch 0 first) and written into page_table[b] after its current pages.
+ *   page_table   host int32 [B][max_pages_per_branch], updated in place.
+ *   prefix_len   multiple of page_size.
+ *   n_used       out (may be NULL): free pages consumed.
+ * Returns FANOUT_EINVAL (table untouched) when a row is too narrow or the
+ * free list too short.
+ */
+FANOUT_API int fanout_extend(int32_t *page_table, int32_t num_branches,
+                int32_t max_pages_per_branch, int32_t prefix_len, const int32_t *suffix_lens,
+                const int32_t *add_lens, int32_t page_size, const int32_t *free_pages,
+                int32_t n_free, int32_t *n_used);
+
+/*
+ * fanout_kv_append -- write new K/V rows into the paged pools (device).
+ * ADR-0060 section 0.5.1 precondition P3: the new tokens' post-RoPE K and V
+ * are in the cache before attention runs. Row r of k_new / v_new is token t of
+ * branch b (rows grouped by branch, branch b has add_lens[b] rows) and is
+ * written, for every KV head h, to
+ *   pool[page_table[b][pos / page_size]][h][pos % page_size][0..d-1],
+ *   pos = prefix_len + suffix_lens[b] + t   (suffix_lens: BEFORE the append).
+ *   k_new, v_new      dev bf16 [R][H_kv][d], 16-byte aligned, d % 8 == 0.
+ *   k_pages, v_pages  dev bf16 [num_pages][H_kv][page_size][d], written.
+ *   page_table        dev int32 [B][max_pages_per_branch] (grown already, e.g.
+ *                     by fanout_extend then copied to the device).
+ * num_branches <= 1024. An out-of-range page id is never written through: the
+ * row is skipped and fanout_last_error() reports FANOUT_EINVAL.
+ */
+FANOUT_API int fanout_kv_append(const void *k_new, const void *v_new, void *k_pages,
+                void *v_pages, const int32_t *page_table, int32_t prefix_len,
+                const int32_t *suffix_lens, const int32_t *add_lens, int32_t num_branches,
+                int32_t max_pages_per_branch, int32_t num_pages, int32_t H_kv, int32_t d,
+                int32_t page_size, fanout_stream_t stream);
+
+/*
  * fanout_attn -- batched shared-prefix fan-out attention.
  * "AHBM Agentic Runtime Architecture" sections 3.2-3.5; "ADR-0060" TL;DR,
  * sections 3, 4, 5.2 and 5.4.
@@ -148,8 +188,9 @@ FANOUT_API int fanout_lse_merge(const float *part_o, const float *part_ml, int32
                      int32_t d, void *out, int32_t out_dtype, float *lse, fanout_stream_t stream);
 
 /* Synchronises `stream`, then returns and clears the device error word of the
- * current device: FANOUT_OK, FANOUT_ETIMEOUT, or FANOUT_ECUDA when the stream
- * itself reports a CUDA error. */
+ * current device: FANOUT_OK, FANOUT_ETIMEOUT (a bounded wait ran out),
+ * FANOUT_EINVAL (fanout_kv_append met a bad page id), or FANOUT_ECUDA when the
+ * stream itself reports a CUDA error. */
 FANOUT_API int fanout_last_error(fanout_stream_t stream);
 
 /* fanout_last_error, also reporting where a device-side wait gave up: `site`
@@ -229,6 +270,12 @@ FANOUT_API int fanout_attn_noalloc(const void *q, const void *k_pages, const voi
                 int32_t max_pages_per_branch, int32_t num_pages, int32_t H_q, int32_t H_kv,
                 int32_t d, int32_t page_size, float scale, int32_t causal, void *out,
                 int32_t out_dtype, float *lse, fanout_stream_t stream);
+
+/* Evaluates, on the device, the software 2^x the attention kernel uses for part
+ * of its softmax exponentials: y[i] = 2^x[i] (dev fp32 arrays of n elements,
+ * x <= 8 expected; x < -126 gives a tiny positive value). Self-test entry:
+ * compares against CUDA's exp2 in the tests. */
+FANOUT_API int fanout_selftest_exp2(const float *x, float *y, int64_t n, fanout_stream_t stream);
 
 /* Frees the workspaces of every device and stream (synchronises first). */
 FANOUT_API int fanout_release(void);

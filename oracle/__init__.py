@@ -69,6 +69,11 @@ def _bind(lib):
     lib.oracle_merge.restype = None
     lib.oracle_count_pairs.argtypes = [i32, i32p, i32p, i32, i32, ctypes.c_int]
     lib.oracle_count_pairs.restype = ctypes.c_int64
+    lib.oracle_extend.argtypes = [i32p, i32, i32, i32, i32p, i32p, i32, i32p, i32]
+    lib.oracle_extend.restype = ctypes.c_int
+    lib.oracle_kv_append.argtypes = [u16p, u16p, u16p, u16p, i32p, i32, i32, i32p, i32p, i32, i32,
+                                     i32, i32]
+    lib.oracle_kv_append.restype = None
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = ctypes.c_int
     return lib
@@ -178,6 +183,35 @@ def count_pairs(prefix_len: int, suffix_lens, q_rows, h_q: int, causal: bool, li
     return int(lib.oracle_count_pairs(int(prefix_len), _p(sl, ctypes.c_int32),
                                       _p(tq, ctypes.c_int32), int(tq.shape[0]), int(h_q),
                                       int(bool(causal))))
+
+
+def extend(table, prefix_len: int, suffix_lens, add_lens, page_size: int, free_pages,
+           lib=None):
+    """Grown copy of the page tables and the number of free pages used."""
+    lib = lib or load()
+    t = np.array(table, dtype=np.int32, copy=True, order="C")
+    sl, al, fr = _i32(suffix_lens), _i32(add_lens), _i32(free_pages)
+    used = lib.oracle_extend(_p(t, ctypes.c_int32), int(t.shape[0]), int(t.shape[1]),
+                             int(prefix_len), _p(sl, ctypes.c_int32), _p(al, ctypes.c_int32),
+                             int(page_size), _p(fr, ctypes.c_int32), int(fr.shape[0]))
+    if used < 0:
+        raise ValueError("oracle_extend: free list or table width too small")
+    return t, int(used)
+
+
+def kv_append(k_new, v_new, k_pool, v_pool, table, prefix_len: int, suffix_lens, add_lens,
+              lib=None):
+    """Pools with the new rows written (copies; inputs untouched)."""
+    lib = lib or load()
+    kn, vn = (np.ascontiguousarray(a, dtype=np.uint16) for a in (k_new, v_new))
+    kp, vp = (np.array(a, dtype=np.uint16, copy=True, order="C") for a in (k_pool, v_pool))
+    t, sl, al = _i32(table), _i32(suffix_lens), _i32(add_lens)
+    _, h_kv, page, d = kp.shape
+    lib.oracle_kv_append(_p(kn, ctypes.c_uint16), _p(vn, ctypes.c_uint16), _p(kp, ctypes.c_uint16),
+                         _p(vp, ctypes.c_uint16), _p(t, ctypes.c_int32), int(t.shape[1]),
+                         int(prefix_len), _p(sl, ctypes.c_int32), _p(al, ctypes.c_int32),
+                         int(t.shape[0]), int(h_kv), int(d), int(page))
+    return kp, vp
 
 
 def run_workload(w, rows=None, lib=None):

@@ -27,6 +27,10 @@
  *     s_j = scale * <q, k_j>, out = sum_j exp(s_j - M) v_j / Z,
  *     M = max_j s_j, Z = sum_j exp(s_j - M); lse = M + ln Z (natural log).
  *     Two passes (max, then exp-sum), all in double from the exact bf16 values.
+ *   - Cache append (ADR-0060, section 0.5.1, precondition P3: the new K/V rows
+ *     are written before attention runs, so attention is a pure read): a
+ *     branch's new tokens go to the next positions of its private suffix,
+ *     with pages taken from the free list as the suffix grows.
  *   - Partial state and merge (ADR-0060, section 4 "Reduction", and
  *     "AHBM Agentic Runtime Architecture" section 3.4): a partial over a key
  *     subset is (m, l, o) with o unnormalised; two partials merge as
@@ -272,6 +276,54 @@ void oracle_merge(const double *parts_m, const double *parts_l, const double *pa
         }
         for (int32_t c = 0; c < d; ++c) acc[c] /= l;
         lse[i] = m + log(l);
+    }
+}
+
+/* Grow branch page tables for new tokens: branch b's private suffix goes from
+ * suffix_lens[b] to suffix_lens[b] + add_lens[b] tokens; the pages it now needs
+ * beyond ceil(suffix_lens[b] / page) come from free_pages in order (branch 0
+ * first) and are written after its current pages. Returns the number of free
+ * pages used, or -1 when the free list or a table row is too short. */
+int oracle_extend(int32_t *table, int32_t num_branches, int32_t max_pages, int32_t prefix_len,
+                  const int32_t *suffix_lens, const int32_t *add_lens, int32_t page_size,
+                  const int32_t *free_pages, int32_t n_free) {
+    int32_t used = 0;
+    int32_t n_pre = prefix_len / page_size;
+    for (int32_t b = 0; b < num_branches; ++b) {
+        int32_t have = (suffix_lens[b] + page_size - 1) / page_size;
+        int32_t need = (suffix_lens[b] + add_lens[b] + page_size - 1) / page_size;
+        if (n_pre + need > max_pages) return -1;
+        for (int32_t i = have; i < need; ++i) {
+            if (used >= n_free) return -1;
+            table[(int64_t)b * max_pages + n_pre + i] = free_pages[used++];
+        }
+    }
+    return used;
+}
+
+/* Write new K/V rows into the paged pool (the cache write that precedes
+ * attention: ADR-0060 section 0.5.1, precondition P3). Row r = token t of
+ * branch b (rows grouped by branch) goes to logical position
+ * prefix_len + suffix_lens[b] + t of branch b, for every KV head.
+ * k_new/v_new [R][H_kv][d]; pools [num_pages][H_kv][page][d]. */
+void oracle_kv_append(const uint16_t *k_new, const uint16_t *v_new, uint16_t *k_pool,
+                      uint16_t *v_pool, const int32_t *table, int32_t max_pages,
+                      int32_t prefix_len, const int32_t *suffix_lens, const int32_t *add_lens,
+                      int32_t num_branches, int32_t H_kv, int32_t d, int32_t page) {
+    int32_t r = 0;
+    for (int32_t b = 0; b < num_branches; ++b) {
+        for (int32_t t = 0; t < add_lens[b]; ++t, ++r) {
+            int32_t j = prefix_len + suffix_lens[b] + t;
+            int32_t phys = table[(int64_t)b * max_pages + j / page];
+            for (int32_t h = 0; h < H_kv; ++h) {
+                int64_t dst = (((int64_t)phys * H_kv + h) * page + (j % page)) * (int64_t)d;
+                int64_t src = ((int64_t)r * H_kv + h) * (int64_t)d;
+                for (int32_t i = 0; i < d; ++i) {
+                    k_pool[dst + i] = k_new[src + i];
+                    v_pool[dst + i] = v_new[src + i];
+                }
+            }
+        }
     }
 }
 

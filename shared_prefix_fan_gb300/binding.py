@@ -25,6 +25,10 @@ _i32, _i64, _f32, _vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c
 _i32p = ctypes.POINTER(ctypes.c_int32)
 ABI = {
     "fanout_fork": (ctypes.c_int, [_i32p, _i32, _i32, _i32p, _i32, _i32p, _i32, _i32p, _i32]),
+    "fanout_extend": (ctypes.c_int, [_i32p, _i32, _i32, _i32, _i32p, _i32p, _i32, _i32p, _i32,
+                                     _i32p]),
+    "fanout_kv_append": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _i32, _i32p, _i32p, _i32, _i32,
+                                        _i32, _i32, _i32, _i32, _vp]),
     "fanout_attn": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _i32p, _i32p, _i32, _i32, _i32, _i32,
                                    _i32, _i32, _i32, _f32, _i32, _vp, _i32, _vp, _vp]),
     "fanout_attn_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _i32p, _i32p, _i32, _i32,
@@ -39,6 +43,7 @@ ABI = {
     "fanout_plan": (ctypes.c_int, [_i32p, _i32p, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32p,
                                    _i32, _i32p, _i32p, _i32, _i32p, _i32p]),
     "fanout_selftest_wait_timeout": (ctypes.c_int, [_i64, _vp]),
+    "fanout_selftest_exp2": (ctypes.c_int, [_vp, _vp, _i64, _vp]),
     "fanout_release": (ctypes.c_int, []),
     "fanout_version": (ctypes.c_char_p, []),
 }
@@ -102,6 +107,33 @@ def fork(prefix_pages, suffix_lens, page_size: int, free_pages, max_pages: int) 
                               _ptr(fr), int(fr.shape[0]), _ptr(table), int(max_pages)),
            "fanout_fork")
     return table[:nb]
+
+
+def extend(page_table, prefix_len: int, suffix_lens, add_lens, page_size: int, free_pages):
+    """Grown copy of host page tables [B][max_pages] and the free pages used."""
+    t = np.array(page_table, dtype=np.int32, copy=True, order="C")
+    sl, al, fr = _i32arr(suffix_lens), _i32arr(add_lens), _i32arr(free_pages)
+    used = ctypes.c_int32(0)
+    _check(load().fanout_extend(_ptr(t), int(t.shape[0]), int(t.shape[1]), int(prefix_len),
+                                _ptr(sl), _ptr(al), int(page_size), _ptr(fr), int(fr.shape[0]),
+                                ctypes.byref(used)), "fanout_extend")
+    return t, int(used.value)
+
+
+def kv_append(k_new, v_new, k_pages, v_pages, page_table, prefix_len: int, suffix_lens,
+              add_lens, page_size: int, stream=None) -> None:
+    """Write new K/V rows [R, H_kv, d] (bf16, device) into the page pools in place."""
+    import torch
+    for name, t in (("k_new", k_new), ("v_new", v_new), ("k_pages", k_pages),
+                    ("v_pages", v_pages)):
+        if t.dtype != torch.bfloat16 or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor")
+    sl, al = _i32arr(suffix_lens), _i32arr(add_lens)
+    _check(load().fanout_kv_append(
+        k_new.data_ptr(), v_new.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(),
+        page_table.data_ptr(), int(prefix_len), _ptr(sl), _ptr(al), int(sl.shape[0]),
+        int(page_table.shape[1]), int(k_pages.shape[0]), int(k_pages.shape[1]),
+        int(k_pages.shape[3]), int(page_size), _stream_handle(stream)), "fanout_kv_append")
 
 
 def plan(suffix_lens, q_rows, prefix_len: int, h_q: int, h_kv: int, page_size: int,
@@ -232,6 +264,15 @@ def set_profile_events(before=None, after=None) -> None:
 
 def selftest_wait_timeout(limit_ns: int = 20_000_000, stream=None) -> int:
     return int(load().fanout_selftest_wait_timeout(int(limit_ns), _stream_handle(stream)))
+
+
+def selftest_exp2(x, stream=None):
+    """The kernels' software 2^x on a CUDA fp32 tensor."""
+    import torch
+    y = torch.empty_like(x)
+    _check(load().fanout_selftest_exp2(x.data_ptr(), y.data_ptr(), x.numel(),
+                                       _stream_handle(stream)), "fanout_selftest_exp2")
+    return y
 
 
 def release() -> None:

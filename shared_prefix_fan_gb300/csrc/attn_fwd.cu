@@ -55,6 +55,7 @@ constexpr int kTileBytes = kBN * kHD * 2;   // one K or V tile, bf16
 constexpr int kHalfBytes = kTileBytes / 2;  // 128 rows x 64 columns (128 B rows)
 constexpr int kQBytes = kBM * kHD * 2;
 constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold (base-2 units)
+constexpr int kPrefetch = 4;          // L2 prefetch distance in K/V tiles (x pages/tile <= 32)
 constexpr int kErrTimeout = 5;        // FANOUT_ETIMEOUT
 
 template <int NQ>
@@ -187,6 +188,27 @@ __device__ void producer_warp(const SplitParams& p, const Smem<NQ>& sm, const CU
                 win_nxt = load_window(win + 1);
             }
             const int pg_off = rel & 31;
+            {
+                // Pull the pages of the tile kPrefetch ahead into L2 now, so its TMA
+                // loads (issued once a ring stage frees up) hit L2.
+                const int jp = j + kPrefetch;
+                if (jp < n_tiles) {
+                    const int relp = jp * ppt;
+                    const int srcv = ((relp >> 5) == win) ? win_cur : win_nxt;
+                    const int n_pgp = (min(kBN, u.key_end - (u.key_begin + jp * kBN)) + ps - 1) / ps;
+                    for (int pg = 0; pg < n_pgp; ++pg) {
+                        // (clamped: an out-of-range id must not become an address)
+                        const int page = min(max(__shfl_sync(0xffffffffu, srcv, (relp & 31) + pg), 0),
+                                             p.num_pages - 1);
+                        if (lane == 0) {
+                            const int64_t off =
+                                (static_cast<int64_t>(page) * p.H_kv + u.kv_head) * ps * 256;
+                            ptx::prefetch_l2(p.k_base + off, static_cast<uint32_t>(ps) * 256u);
+                            ptx::prefetch_l2(p.v_base + off, static_cast<uint32_t>(ps) * 256u);
+                        }
+                    }
+                }
+            }
             for (int kv = 0; kv < 2 && ok; ++kv, ++it) {
                 const uint32_t stage = it % C::kStages;
                 const uint32_t par = (it / C::kStages) & 1u;
@@ -402,6 +424,54 @@ __device__ __forceinline__ float sum8(const float (&a)[8]) {
     return ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
 }
 
+// Second softmax pass over one S buffer in TMEM: exponentials, row-sum
+// partials, and P as bf16 pairs stored over the first 64 columns (chunk pair h
+// of S -> P columns 32h .. 32h+31, all already read). In fully visible tiles
+// every kPolyEvery-th pair of columns uses the software exp2 on the FMA pipe
+// and the rest the MUFU ex2, which splits the exponential work between the
+// two units; masked tiles use ex2 only (exact zeros for masked columns).
+constexpr int kPolyEvery = 4;
+
+template <bool FULL>
+__device__ __forceinline__ void softmax_pass2(uint32_t s_addr, int lim_c, float sl2, float m_use,
+                                              float (&sm8)[8]) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+            uint32_t a[32];
+            ptx::tmem_ld32(s_addr + 64 * h + 32 * part, a);
+            ptx::tmem_ld_wait(a);
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+                const int c = 64 * h + 32 * part + i;
+                float e0, e1;
+                if (FULL) {
+                    const float y0 = fmaf(__uint_as_float(a[i]), sl2, -m_use);
+                    const float y1 = fmaf(__uint_as_float(a[i + 1]), sl2, -m_use);
+                    if (((i >> 1) % kPolyEvery) == kPolyEvery - 1) {
+                        e0 = ptx::ex2_poly(y0);
+                        e1 = ptx::ex2_poly(y1);
+                    } else {
+                        e0 = ptx::ex2(y0);
+                        e1 = ptx::ex2(y1);
+                    }
+                } else {
+                    const float x0 = (c < lim_c) ? __uint_as_float(a[i]) : -INFINITY;
+                    const float x1 = (c + 1 < lim_c) ? __uint_as_float(a[i + 1]) : -INFINITY;
+                    e0 = ptx::ex2(fmaf(x0, sl2, -m_use));
+                    e1 = ptx::ex2(fmaf(x1, sl2, -m_use));
+                }
+                sm8[i & 7] += e0;
+                sm8[(i + 1) & 7] += e1;
+                pk[16 * part + (i >> 1)] = ptx::pack_bf16x2(e0, e1);
+            }
+        }
+        ptx::tmem_st32(s_addr + 32 * h, pk);
+    }
+}
+
 // Group x owns query tile x of every unit (rows 128x .. 128x+127); thread i
 // owns row i of the tile (TMEM lane i). A warp whose 32 rows are all padding
 // follows the barrier protocol but skips the TMEM traffic and the math.
@@ -476,27 +546,10 @@ __device__ void softmax_group(const SplitParams& p, const Smem<NQ>& sm, uint32_t
                 float sm8[8];
 #pragma unroll
                 for (int q = 0; q < 8; ++q) sm8[q] = 0.f;
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t pk[32];
-#pragma unroll
-                    for (int part = 0; part < 2; ++part) {
-                        uint32_t a[32];
-                        ptx::tmem_ld32(lane_addr + colS + 64 * h + 32 * part, a);
-                        ptx::tmem_ld_wait(a);
-#pragma unroll
-                        for (int i = 0; i < 32; i += 2) {
-                            const int c = 64 * h + 32 * part + i;
-                            const float x0 = (full || c < lim_c) ? __uint_as_float(a[i]) : -INFINITY;
-                            const float x1 = (full || c + 1 < lim_c) ? __uint_as_float(a[i + 1]) : -INFINITY;
-                            const float e0 = ptx::ex2(fmaf(x0, sl2, -m_use));
-                            const float e1 = ptx::ex2(fmaf(x1, sl2, -m_use));
-                            sm8[i & 7] += e0;
-                            sm8[(i + 1) & 7] += e1;
-                            pk[16 * part + (i >> 1)] = ptx::pack_bf16x2(e0, e1);
-                        }
-                    }
-                    ptx::tmem_st32(lane_addr + colS + 32 * h, pk);
+                if (full) {
+                    softmax_pass2<true>(lane_addr + colS, 0, sl2, m_use, sm8);
+                } else {
+                    softmax_pass2<false>(lane_addr + colS, lim_c, sl2, m_use, sm8);
                 }
                 l_run = l_run * corr + sum8(sm8);
                 ptx::tmem_st_wait();

@@ -104,6 +104,77 @@ int fanout_fork(const int32_t* prefix_pages, int32_t n_prefix_pages, int32_t num
     return FANOUT_OK;
 }
 
+int fanout_extend(int32_t* page_table, int32_t num_branches, int32_t max_pages_per_branch,
+                  int32_t prefix_len, const int32_t* suffix_lens, const int32_t* add_lens,
+                  int32_t page_size, const int32_t* free_pages, int32_t n_free, int32_t* n_used) {
+    if (num_branches < 0 || max_pages_per_branch < 0 || prefix_len < 0 || page_size <= 0 ||
+        n_free < 0 || prefix_len % page_size != 0)
+        return FANOUT_EINVAL;
+    if (num_branches > 0 && (!page_table || !suffix_lens || !add_lens)) return FANOUT_EINVAL;
+    if (n_free > 0 && !free_pages) return FANOUT_EINVAL;
+    const int64_t n_pre = prefix_len / page_size;
+    int64_t used = 0;
+    for (int32_t b = 0; b < num_branches; ++b) {
+        if (suffix_lens[b] < 0 || add_lens[b] < 0) return FANOUT_EINVAL;
+        const int64_t have = (static_cast<int64_t>(suffix_lens[b]) + page_size - 1) / page_size;
+        const int64_t need =
+            (static_cast<int64_t>(suffix_lens[b]) + add_lens[b] + page_size - 1) / page_size;
+        if (n_pre + need > max_pages_per_branch) return FANOUT_EINVAL;
+        if (used + (need - have) > n_free) return FANOUT_EINVAL;
+    }
+    for (int32_t b = 0; b < num_branches; ++b) {  // checked first: no partial update on error
+        const int64_t have = (static_cast<int64_t>(suffix_lens[b]) + page_size - 1) / page_size;
+        const int64_t need =
+            (static_cast<int64_t>(suffix_lens[b]) + add_lens[b] + page_size - 1) / page_size;
+        for (int64_t i = have; i < need; ++i)
+            page_table[static_cast<int64_t>(b) * max_pages_per_branch + n_pre + i] =
+                free_pages[used++];
+    }
+    if (n_used) *n_used = static_cast<int32_t>(used);
+    return FANOUT_OK;
+}
+
+int fanout_kv_append(const void* k_new, const void* v_new, void* k_pages, void* v_pages,
+                     const int32_t* page_table, int32_t prefix_len, const int32_t* suffix_lens,
+                     const int32_t* add_lens, int32_t num_branches, int32_t max_pages_per_branch,
+                     int32_t num_pages, int32_t H_kv, int32_t d, int32_t page_size,
+                     fanout_stream_t stream) {
+    if (num_branches < 0 || prefix_len < 0 || H_kv <= 0 || d <= 0 || page_size <= 0 ||
+        num_pages <= 0 || max_pages_per_branch <= 0)
+        return FANOUT_EINVAL;
+    if (num_branches > kMaxAppendBranches || d % 8 != 0 || d > 1024) return FANOUT_EUNSUPPORTED;
+    if (num_branches > 0 && (!suffix_lens || !add_lens)) return FANOUT_EINVAL;
+    AppendParams p;
+    p.num_branches = num_branches;
+    p.H_kv = H_kv;
+    p.d = d;
+    p.page_size = page_size;
+    p.max_pages = max_pages_per_branch;
+    p.num_pages = num_pages;
+    p.prefix_len = prefix_len;
+    int64_t R = 0;
+    for (int32_t b = 0; b < num_branches; ++b) {
+        if (suffix_lens[b] < 0 || add_lens[b] < 0) return FANOUT_EINVAL;
+        const int64_t end = static_cast<int64_t>(prefix_len) + suffix_lens[b] + add_lens[b];
+        if ((end + page_size - 1) / page_size > max_pages_per_branch) return FANOUT_EINVAL;
+        p.row_off[b] = static_cast<int32_t>(R);
+        p.suffix_len[b] = suffix_lens[b];
+        R += add_lens[b];
+    }
+    if (R == 0) return FANOUT_OK;
+    if (R * H_kv > (1LL << 31)) return FANOUT_EUNSUPPORTED;
+    p.row_off[num_branches] = static_cast<int32_t>(R);
+    p.R = static_cast<int32_t>(R);
+    if (!k_new || !v_new || !k_pages || !v_pages || !page_table) return FANOUT_EINVAL;
+    if (!ok_align16(k_new) || !ok_align16(v_new) || !ok_align16(k_pages) || !ok_align16(v_pages))
+        return FANOUT_EINVAL;
+    int32_t* err = nullptr;
+    cudaError_t ce = err_word_ptr(&err);
+    if (ce != cudaSuccess) return status_from_cuda(ce);
+    return status_from_cuda(launch_kv_append(k_new, v_new, k_pages, v_pages, page_table, p, err,
+                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int fanout_set_option(int32_t option, int64_t value) {
     std::lock_guard<std::mutex> lk(g_mu);
     switch (option) {
@@ -298,6 +369,11 @@ int fanout_selftest_wait_timeout(int64_t limit_ns, fanout_stream_t stream) {
                               reinterpret_cast<cudaStream_t>(stream));
     if (ce != cudaSuccess) return status_from_cuda(ce);
     return fanout_last_error(stream);
+}
+
+int fanout_selftest_exp2(const float* x, float* y, int64_t n, fanout_stream_t stream) {
+    if (n < 0 || (n > 0 && (!x || !y))) return FANOUT_EINVAL;
+    return status_from_cuda(launch_exp2_selftest(x, y, n, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int fanout_release(void) {

@@ -64,6 +64,8 @@ int build_plan(const PlanInput& in, Plan& plan);
 
 struct SplitParams {
     const int32_t* page_table;
+    const uint8_t* k_base;  // page pools (for L2 prefetches ahead of the TMA loads)
+    const uint8_t* v_base;
     const Unit* units;
     const int32_t* cta_first;
     float* part_o;    // [part][128 * nq rows][kHD]
@@ -72,6 +74,7 @@ struct SplitParams {
     float* lse;       // [R][H_q] or null
     int32_t* err;     // device error word
     int32_t max_pages;
+    int32_t num_pages;  // pool pages: clamps prefetch addresses of bad page ids
     int32_t R, H_q, H_kv, G, page_size, tpt;
     int32_t nq;        // query tiles per unit: selects the kernel instance
     int32_t out_bf16;
@@ -129,12 +132,25 @@ int validate_call(const void* q, const void* k, const void* v, const int32_t* pa
                   int32_t num_pages, int32_t page_size, float scale, int32_t out_dtype,
                   const void* out);
 
+// Paged KV append: per-branch row offsets and current suffix lengths travel in
+// the kernel parameters (no workspace).
+constexpr int kMaxAppendBranches = 1024;
+struct AppendParams {
+    int32_t num_branches, R, H_kv, d, page_size, max_pages, num_pages, prefix_len;
+    int32_t row_off[kMaxAppendBranches + 1];  // first row of each branch (+ total)
+    int32_t suffix_len[kMaxAppendBranches];   // suffix length before the append
+};
+
 // Launchers (defined in the .cu files); return cudaError_t.
 cudaError_t launch_split_attn(const SplitParams& p, const CUtensorMap& tm_q,
                               const CUtensorMap& tm_k, const CUtensorMap& tm_v, int grid,
                               cudaStream_t stream);
 cudaError_t launch_lse_merge(const MergeParams& p, cudaStream_t stream);
 cudaError_t err_word_ptr(int32_t** ptr);
+cudaError_t launch_kv_append(const void* k_new, const void* v_new, void* k_pool, void* v_pool,
+                             const int32_t* page_table, const AppendParams& p, int32_t* err,
+                             cudaStream_t stream);
+cudaError_t launch_exp2_selftest(const float* x, float* y, int64_t n, cudaStream_t stream);
 cudaError_t launch_wait_selftest(int32_t* err, unsigned long long limit_ns, cudaStream_t stream);
 
 }  // namespace fanout

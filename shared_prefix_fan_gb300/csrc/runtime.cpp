@@ -160,6 +160,8 @@ int launch_plan(const CallArgs& a, const Plan& pl, const Layout& L, uint8_t* bas
 
     SplitParams p;
     p.page_table = a.page_table;
+    p.k_base = static_cast<const uint8_t*>(a.k);
+    p.v_base = static_cast<const uint8_t*>(a.v);
     p.units = reinterpret_cast<const Unit*>(base + L.units);
     p.cta_first = reinterpret_cast<const int32_t*>(base + L.cta);
     p.part_o = reinterpret_cast<float*>(base + L.o);
@@ -168,6 +170,7 @@ int launch_plan(const CallArgs& a, const Plan& pl, const Layout& L, uint8_t* bas
     p.lse = a.lse;
     p.err = err;
     p.max_pages = a.max_pages;
+    p.num_pages = a.num_pages;
     p.R = static_cast<int32_t>(a.R);
     p.H_q = a.H_q;
     p.H_kv = a.H_kv;

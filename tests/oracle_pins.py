@@ -316,6 +316,51 @@ def pin_work_identity(lib):
     assert oracle.count_pairs(P, S, T, 64, causal=True, lib=lib) == 64 * c
 
 
+def pin_append(lib, seed=9):
+    """Fork for the current suffixes, then grow the tables and append the new
+    tokens' K/V: every logical key of every branch must then read back its own
+    row (checked by a gather written here), and attention must match brute
+    force on the grown contexts (ADR-0060 section 0.5.1, precondition P3)."""
+    rng = np.random.default_rng(seed)
+    for (P, S_old, T, page) in (([32], [5, 16, 0], [3, 1, 4], 8), ([0], [7, 1], [2, 9], 4)):
+        P = P[0]
+        S_new = [a + b for a, b in zip(S_old, T)]
+        pb = Problem(rng, len(T), P, S_new, T, 8, 2, 16, page, True)
+        # the state before the append: a pool holding only the old tokens
+        n_pre = P // page
+        max_pages = pb.max_pages
+        free = rng.permutation(np.arange(2000, 2000 + 200, dtype=np.int32))
+        table0 = oracle.fork(np.arange(1000, 1000 + n_pre, dtype=np.int32), S_old, page, free,
+                             max_pages, lib=lib)
+        n_used0 = sum((s + page - 1) // page for s in S_old)
+        pool_pages = 2200
+        kp = np.zeros((pool_pages, pb.h_kv, page, pb.d), np.uint16)
+        vp = np.zeros_like(kp)
+        for b in range(pb.B):
+            for j in range(P + S_old[b]):
+                pg = table0[b, j // page]
+                kp[pg, :, j % page] = pb.k_log[b][j]
+                vp[pg, :, j % page] = pb.v_log[b][j]
+        table1, used = oracle.extend(table0, P, S_old, T, page, free[n_used0:], lib=lib)
+        assert used == sum((s + t + page - 1) // page - (s + page - 1) // page
+                           for s, t in zip(S_old, T))
+        grown = table1[table1 >= 0]
+        assert len(np.unique(grown[grown >= 2000])) == len(grown[grown >= 2000])
+        k_new = np.concatenate([pb.k_log[b][P + S_old[b]:] for b in range(pb.B)])
+        v_new = np.concatenate([pb.v_log[b][P + S_old[b]:] for b in range(pb.B)])
+        kp1, vp1 = oracle.kv_append(k_new, v_new, kp, vp, table1, P, S_old, T, lib=lib)
+        for b in range(pb.B):
+            for j in range(P + S_new[b]):
+                pg = table1[b, j // page]
+                assert (kp1[pg, :, j % page] == pb.k_log[b][j]).all(), (b, j)
+                assert (vp1[pg, :, j % page] == pb.v_log[b][j]).all(), (b, j)
+        out, lse = oracle.attn(pb.q, kp1, vp1, table1, P, S_new, T, pb.h_q, pb.h_kv, page,
+                               pb.scale, True, lib=lib)
+        bo, bl = pb.brute()
+        _close(out, bo, 1e-12)
+        _close(lse, bl, 1e-12)
+
+
 ALL_PINS = [pin_brute_force, pin_identical_keys, pin_single_key, pin_batching_invariance,
             pin_merge_invariance, pin_gqa_invariance, pin_fork_invariance,
-            pin_causal_reductions, pin_fork, pin_work_identity]
+            pin_causal_reductions, pin_fork, pin_work_identity, pin_append]

@@ -1,0 +1,67 @@
+"""fanout_kv_append on the GPU against the oracle's append (bit-exact pools), and
+the whole step a decoding fan-out runs -- fork, grow the tables, append the
+new tokens' K/V, attend -- against the oracle doing the same."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from shared_prefix_fan_gb300 import binding
+from shared_prefix_fan_gb300.workloads import _bf16_bits, draw, small_spec
+from tests.gpu_helpers import compare, ensure_lib, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("case", range(3))
+def test_fork_extend_append_attend(case):
+    ensure_lib()
+    tq, s_old, P, ps, hq, hkv = [
+        ([1] * 8, [500] * 8, 1024, 64, 64, 8),
+        ([3, 0, 17, 5], [13, 40, 0, 77], 256, 16, 16, 2),
+        ([20, 20], [236, 100], 512, 32, 32, 4),
+    ][case]
+    s_new = [a + b for a, b in zip(s_old, tq)]
+    spec = small_spec(h_q=hq, h_kv=hkv, page_size=ps, prefix_len=P, q_rows=tq,
+                      suffix_lens=s_new, permute_prefix=True, permute_suffix=True, seed=300 + case)
+    w = draw(spec)  # pool sized for the grown suffixes; the drawn values are the "old" cache
+    rng = np.random.default_rng(case)
+    R = int(sum(tq))
+    k_new = _bf16_bits(torch.from_numpy(rng.standard_normal((R, hkv, 128)).astype(np.float32)))
+    v_new = _bf16_bits(torch.from_numpy(rng.standard_normal((R, hkv, 128)).astype(np.float32)))
+    n_pre = P // ps
+    mp = w.max_pages_per_branch
+    n_old = sum((s + ps - 1) // ps for s in s_old)
+    # product: fork for the old suffixes, grow, append on the device
+    t0 = binding.fork(w.prefix_pages, s_old, ps, w.free_pages, mp)
+    t1, used = binding.extend(t0, P, s_old, tq, ps, w.free_pages[n_old:])
+    k_pool, v_pool = to_dev_bf16(w.k_pool), to_dev_bf16(w.v_pool)
+    dt1 = torch.from_numpy(t1).cuda()
+    binding.kv_append(to_dev_bf16(k_new), to_dev_bf16(v_new), k_pool, v_pool, dt1, P, s_old, tq,
+                      ps)
+    assert binding.last_error() == binding.OK
+    # oracle: the same steps on the host
+    r0 = oracle.fork(w.prefix_pages, s_old, ps, w.free_pages, mp)
+    r1, used_ref = oracle.extend(r0, P, s_old, tq, ps, w.free_pages[n_old:])
+    assert np.array_equal(t1, r1) and used == used_ref
+    rk, rv = oracle.kv_append(k_new, v_new, w.k_pool, w.v_pool, r1, P, s_old, tq)
+    gk = k_pool.view(torch.int16).cpu().numpy().view(np.uint16)
+    gv = v_pool.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.array_equal(gk, rk) and np.array_equal(gv, rv)
+    # attention over the grown contexts, the new tokens attending as the suffix tail
+    q = to_dev_bf16(w.q)
+    out, lse = binding.attn(q, k_pool, v_pool, dt1, P, s_new, tq, hq, hkv, ps, spec.scale, True)
+    assert binding.last_error() == binding.OK
+    ro, rl = oracle.attn(w.q, rk, rv, r1, P, s_new, tq, hq, hkv, ps, spec.scale, True)
+    compare(out, lse, ro, rl, what=f"append case {case}")
+
+
+def test_kv_append_skips_bad_page_ids():
+    ensure_lib()
+    k_pool = torch.zeros((4, 1, 16, 128), dtype=torch.bfloat16, device="cuda")
+    v_pool = torch.zeros_like(k_pool)
+    table = torch.tensor([[0, 99]], dtype=torch.int32, device="cuda")  # page 99 does not exist
+    k_new = torch.ones((1, 1, 128), dtype=torch.bfloat16, device="cuda")
+    binding.kv_append(k_new, k_new.clone(), k_pool, v_pool, table, 0, [16], [1], 16)
+    assert binding.last_error() == binding.EINVAL
+    assert (k_pool == 0).all() and (v_pool == 0).all()

@@ -28,6 +28,10 @@ MUTATIONS = [
     ("fork_reuses_pages", "free_pages[next_free++]", "free_pages[i]"),
     ("v_used_as_k", "const uint16_t *kr = kv_row(pb->k,", "const uint16_t *kr = kv_row(pb->v,"),
     ("softmax_denominator_dropped", "dst[c] = o[c] / l;", "dst[c] = o[c];"),
+    ("append_position_shifted", "int32_t j = prefix_len + suffix_lens[b] + t;",
+     "int32_t j = prefix_len + suffix_lens[b] + t + 1;"),
+    ("extend_floor_pages", "int32_t have = (suffix_lens[b] + page_size - 1) / page_size;",
+     "int32_t have = suffix_lens[b] / page_size;"),
 ]
 
 
@@ -42,6 +46,6 @@ def test_planted_mistake_is_caught(name, orig, bad, tmp_path):
     for pin in oracle_pins.ALL_PINS:
         try:
             pin(lib)
-        except (AssertionError, ValueError) as e:
+        except (AssertionError, ValueError, IndexError) as e:
             failures.append(pin.__name__)
     assert failures, f"planted mistake {name} passed every pin"
