@@ -227,6 +227,21 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------ ranks
+def max_over_ranks(values, dist=None, device="cpu"):
+    """Element-wise max of per-rank timings (all ranks get the result).
+
+    Replicas: every rank runs the whole problem on its own GPU; the slowest
+    rank defines the job's time."""
+    if dist is None or not dist.is_available() or not dist.is_initialized() \
+            or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    import torch
+    x = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(x, op=dist.ReduceOp.MAX)
+    return x.tolist()
+
+
 # ------------------------------------------------------------------ GPU arm
 def main():
     ap = argparse.ArgumentParser()
@@ -331,10 +346,8 @@ def main():
         raise RuntimeError(f"device error {binding.strerror(rc)}")
     mean_call = float(call_ms.mean())
     mean_split = float(split_ms.mean())
-    if world > 1:
-        x = torch.tensor([mean_call, mean_split], device="cuda", dtype=torch.float64)
-        dist.all_reduce(x, op=dist.ReduceOp.MAX)
-        mean_call, mean_split = x.tolist()
+    mean_call, mean_split = max_over_ranks([mean_call, mean_split], dist if world > 1 else None,
+                                           "cuda")
 
     # end to end: inputs from pinned host memory, result read back, every step
     e2e = None
@@ -360,10 +373,7 @@ def main():
             if i >= 2:
                 e2e_ms.append(a.elapsed_time(b))
         e2e_val = float(np.mean(e2e_ms)) * 1e3
-        if world > 1:
-            x = torch.tensor([e2e_val], device="cuda", dtype=torch.float64)
-            dist.all_reduce(x, op=dist.ReduceOp.MAX)
-            e2e_val = x.item()
+        e2e_val = max_over_ranks([e2e_val], dist if world > 1 else None, "cuda")[0]
         h2d = sum(x.numel() * x.element_size() for x in (p_q, p_k, p_v, p_t))
         d2h = sum(x.numel() * x.element_size() for x in (p_out, p_lse))
         e2e = {"value": e2e_val, "unit": "us/call", "h2d_bytes_per_step": int(h2d),
