@@ -33,9 +33,10 @@ namespace {
 // load together; then up to kMergeBatch partials per pass: lane e loads entry
 // e's (m, l) while every lane loads its 4 columns of all the pass's O vectors,
 // so a row of up to kMergeBatch partials costs two memory round trips.
-constexpr int kMergeBatch = 24;
-
-__global__ void __launch_bounds__(256, 1) lse_merge_kernel(const MergeParams p) {
+// kMergeBatch partials per pass: 24 for rows with many partials (decode), 8 when
+// every row has few (a smaller register footprint keeps three blocks per SM).
+template <int kMergeBatch, int kMinBlocks>
+__global__ void __launch_bounds__(256, kMinBlocks) lse_merge_kernel(const MergeParams p) {
     // Launched as a programmatic dependent of the attention kernel: wait until
     // that grid has completed and its writes are visible.
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -154,6 +155,7 @@ cudaError_t launch_lse_merge(const MergeParams& p, cudaStream_t stream) {
         static_cast<int>(std::min<int64_t>(blocks_needed, static_cast<int64_t>(sms) * 16));
     // Programmatic dependent launch: the merge grid may start while the
     // attention kernel finishes; griddepcontrol.wait orders the reads.
+    const int32_t most = p.merge_cnt ? p.merge_stride : p.n_parts;  // partials of the fullest row
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(256);
@@ -164,7 +166,8 @@ cudaError_t launch_lse_merge(const MergeParams& p, cudaStream_t stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, lse_merge_kernel, p);
+    if (most <= 8) return cudaLaunchKernelEx(&cfg, lse_merge_kernel<8, 3>, p);
+    return cudaLaunchKernelEx(&cfg, lse_merge_kernel<24, 1>, p);
 }
 
 // Device address of this device's error word (the symbol's host-side name is
