@@ -84,6 +84,43 @@ FANOUT_API int fanout_fork(const int32_t *prefix_pages, int32_t n_prefix_pages, 
                 int32_t n_free, int32_t *page_table, int32_t max_pages_per_branch);
 
 /*
+ * fanout_fork_cow -- fork when the prefix ends inside a page (host only).
+ * "AHBM Agentic Runtime Architecture" section 3.1: shared pages are
+ * referenced, never copied -- but a partially filled last prefix page cannot
+ * be shared by branches that will each append after it, so every branch gets
+ * its own copy of that one page (copy-on-write at fork time).
+ *   prefix_pages  host int32 [ceil(prefix_len / page_size)] physical ids.
+ *   page_table    host int32 [B][max_pages_per_branch], written: the whole
+ *                 prefix pages (shared), then the branch's own pages -- first
+ *                 the copy of the partial prefix page, if any, then its suffix
+ *                 pages -- taken from free_pages in order, branch 0 first;
+ *                 then -1.
+ *   cow_pairs     host int32 [B][2] or NULL: {source page, branch's copy} per
+ *                 branch when the prefix ends inside a page (unwritten
+ *                 otherwise); copy them with fanout_copy_pages (rows =
+ *                 prefix_len % page_size) before appending.
+ *   n_used        out (may be NULL): free pages consumed.
+ * With prefix_len a multiple of page_size this is fanout_fork. Returns
+ * FANOUT_EINVAL (table untouched) when the free list or a row is too short.
+ */
+FANOUT_API int fanout_fork_cow(const int32_t *prefix_pages, int32_t prefix_len,
+                int32_t num_branches, const int32_t *suffix_lens, int32_t page_size,
+                const int32_t *free_pages, int32_t n_free, int32_t *page_table,
+                int32_t max_pages_per_branch, int32_t *cow_pairs, int32_t *n_used);
+
+/*
+ * fanout_copy_pages -- copy token slots [0, rows) of page pairs[i][0] to page
+ * pairs[i][1], every KV head, in both pools (device). The copy-on-write step
+ * of fanout_fork_cow.
+ *   pairs   dev int32 [n_pairs][2]; pools dev bf16 [num_pages][H_kv][page][d].
+ * A page id outside [0, num_pages) is never used: the pair is skipped and
+ * fanout_last_error() reports FANOUT_EINVAL.
+ */
+FANOUT_API int fanout_copy_pages(void *k_pages, void *v_pages, const int32_t *pairs,
+                int32_t n_pairs, int32_t rows, int32_t num_pages, int32_t H_kv, int32_t d,
+                int32_t page_size, fanout_stream_t stream);
+
+/*
  * fanout_extend -- grow branch page tables for new tokens (host only).
  * "AHBM Agentic Runtime Architecture" section 3.1 (private suffix pages per
  * branch); ADR-0060 section 0.5.1 precondition P3 (the cache grows before
@@ -143,7 +180,10 @@ FANOUT_API int fanout_kv_append(const void *k_new, const void *v_new, void *k_pa
  *   k_pages, v_pages dev bf16 [num_pages][H_kv][page_size][d]. 16-byte aligned.
  *   page_table       dev int32 [num_branches][max_pages_per_branch]; every
  *                    entry a branch reads must be in [0, num_pages).
- *   prefix_len       tokens, a multiple of page_size (>= 0).
+ *   prefix_len       tokens (>= 0). When it is not a multiple of page_size,
+ *                    the whole pages are read as the shared prefix and the
+ *                    rest of the last prefix page through each branch's own
+ *                    table entry (a private copy after fanout_fork_cow).
  *   suffix_lens      HOST int32 [num_branches] (>= 0).
  *   q_rows_per_branch HOST int32 [num_branches] (>= 0); with causal != 0 each
  *                    must be <= suffix_lens[b].
@@ -157,7 +197,9 @@ FANOUT_API int fanout_kv_append(const void *k_new, const void *v_new, void *k_pa
  *   lse              dev fp32 [R][H_q] or NULL: natural-log log-sum-exp of the
  *                    scaled visible scores, m + ln(l).
  *   stream           stream the work is ordered on.
- * Host-side validation reads only host arrays; page-table entries are read by
+ * The shared prefix: entries [0, prefix_len / page_size) (whole pages) of
+ * every row must be the same page ids; shared-prefix work reads them through
+ * row 0. Host-side validation reads only host arrays; page-table entries are read by
  * the kernel (set option FANOUT_OPT_VALIDATE_TABLE to check them on the host
  * with a device-to-host copy first). R == 0 is a no-op returning FANOUT_OK.
  * The library keeps a grow-only device workspace per (device, stream) for

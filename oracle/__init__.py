@@ -69,6 +69,10 @@ def _bind(lib):
     lib.oracle_merge.restype = None
     lib.oracle_count_pairs.argtypes = [i32, i32p, i32p, i32, i32, ctypes.c_int]
     lib.oracle_count_pairs.restype = ctypes.c_int64
+    lib.oracle_fork_cow.argtypes = [i32p, i32, i32, i32p, i32, i32p, i32, i32p, i32, i32p]
+    lib.oracle_fork_cow.restype = ctypes.c_int
+    lib.oracle_copy_pages.argtypes = [u16p, u16p, i32p, i32, i32, i32, i32, i32]
+    lib.oracle_copy_pages.restype = None
     lib.oracle_extend.argtypes = [i32p, i32, i32, i32, i32p, i32p, i32, i32p, i32]
     lib.oracle_extend.restype = ctypes.c_int
     lib.oracle_kv_append.argtypes = [u16p, u16p, u16p, u16p, i32p, i32, i32, i32p, i32p, i32, i32,
@@ -183,6 +187,35 @@ def count_pairs(prefix_len: int, suffix_lens, q_rows, h_q: int, causal: bool, li
     return int(lib.oracle_count_pairs(int(prefix_len), _p(sl, ctypes.c_int32),
                                       _p(tq, ctypes.c_int32), int(tq.shape[0]), int(h_q),
                                       int(bool(causal))))
+
+
+def fork_cow(prefix_pages, prefix_len: int, suffix_lens, page_size: int, free_pages,
+             max_pages: int, lib=None):
+    """(tables [B][max_pages], cow pairs [B][2], free pages used)."""
+    lib = lib or load()
+    pre, sl, fr = _i32(prefix_pages), _i32(suffix_lens), _i32(free_pages)
+    nb = int(sl.shape[0])
+    table = np.full((max(nb, 1), max_pages), -1, dtype=np.int32)
+    cow = np.full((max(nb, 1), 2), -1, dtype=np.int32)
+    used = lib.oracle_fork_cow(_p(pre, ctypes.c_int32), int(prefix_len), nb,
+                               _p(sl, ctypes.c_int32), int(page_size), _p(fr, ctypes.c_int32),
+                               int(fr.shape[0]), _p(table, ctypes.c_int32), int(max_pages),
+                               _p(cow, ctypes.c_int32))
+    if used < 0:
+        raise ValueError("oracle_fork_cow: free list or table width too small")
+    return table[:nb], cow[:nb], int(used)
+
+
+def copy_pages(k_pool, v_pool, pairs, rows: int, lib=None):
+    """Copies of the pools with token slots [0, rows) of each pair's page copied."""
+    lib = lib or load()
+    kp, vp = (np.array(a, dtype=np.uint16, copy=True, order="C") for a in (k_pool, v_pool))
+    pr = _i32(pairs).reshape(-1, 2)
+    _, h_kv, page, d = kp.shape
+    lib.oracle_copy_pages(_p(kp, ctypes.c_uint16), _p(vp, ctypes.c_uint16),
+                          _p(pr, ctypes.c_int32), int(pr.shape[0]), int(rows), int(h_kv),
+                          int(page), int(d))
+    return kp, vp
 
 
 def extend(table, prefix_len: int, suffix_lens, add_lens, page_size: int, free_pages,

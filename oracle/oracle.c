@@ -279,6 +279,53 @@ void oracle_merge(const double *parts_m, const double *parts_l, const double *pa
     }
 }
 
+/* Fork when the prefix may end inside a page: the whole prefix pages are
+ * shared; a partially filled last prefix page is given to each branch as its
+ * own copy (a fresh page from the free list, filled by oracle_copy_pages),
+ * followed by the branch's suffix pages; pages are taken in order, branch 0
+ * first. cow[b] = {shared partial page, branch's copy} when the prefix ends
+ * inside a page. Returns the number of free pages used, or -1. */
+int oracle_fork_cow(const int32_t *prefix_pages, int32_t prefix_len, int32_t num_branches,
+                    const int32_t *suffix_lens, int32_t page_size, const int32_t *free_pages,
+                    int32_t n_free, int32_t *table, int32_t max_pages, int32_t *cow) {
+    int32_t n_full = prefix_len / page_size;
+    int32_t partial = (prefix_len % page_size) != 0;
+    int32_t used = 0;
+    for (int32_t b = 0; b < num_branches; ++b) {
+        int32_t need = (prefix_len + suffix_lens[b] + page_size - 1) / page_size;
+        if (need < n_full + partial) need = n_full + partial;
+        if (need > max_pages) return -1;
+        int32_t *row = table + (int64_t)b * max_pages;
+        for (int32_t i = 0; i < max_pages; ++i) row[i] = -1;
+        for (int32_t i = 0; i < n_full; ++i) row[i] = prefix_pages[i];
+        for (int32_t i = n_full; i < need; ++i) {
+            if (used >= n_free) return -1;
+            row[i] = free_pages[used++];
+        }
+        if (partial) {
+            cow[2 * b] = prefix_pages[n_full];
+            cow[2 * b + 1] = row[n_full];
+        }
+    }
+    return used;
+}
+
+/* Copy token slots [0, rows) of page pairs[i][0] to page pairs[i][1] (every
+ * KV head, both pools). */
+void oracle_copy_pages(uint16_t *k_pool, uint16_t *v_pool, const int32_t *pairs, int32_t n_pairs,
+                       int32_t rows, int32_t H_kv, int32_t page, int32_t d) {
+    for (int32_t i = 0; i < n_pairs; ++i)
+        for (int32_t h = 0; h < H_kv; ++h)
+            for (int32_t s = 0; s < rows; ++s) {
+                int64_t src = (((int64_t)pairs[2 * i] * H_kv + h) * page + s) * (int64_t)d;
+                int64_t dst = (((int64_t)pairs[2 * i + 1] * H_kv + h) * page + s) * (int64_t)d;
+                for (int32_t c = 0; c < d; ++c) {
+                    k_pool[dst + c] = k_pool[src + c];
+                    v_pool[dst + c] = v_pool[src + c];
+                }
+            }
+}
+
 /* Grow branch page tables for new tokens: branch b's private suffix goes from
  * suffix_lens[b] to suffix_lens[b] + add_lens[b] tokens; the pages it now needs
  * beyond ceil(suffix_lens[b] / page) come from free_pages in order (branch 0

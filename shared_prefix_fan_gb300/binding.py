@@ -25,6 +25,9 @@ _i32, _i64, _f32, _vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c
 _i32p = ctypes.POINTER(ctypes.c_int32)
 ABI = {
     "fanout_fork": (ctypes.c_int, [_i32p, _i32, _i32, _i32p, _i32, _i32p, _i32, _i32p, _i32]),
+    "fanout_fork_cow": (ctypes.c_int, [_i32p, _i32, _i32, _i32p, _i32, _i32p, _i32, _i32p, _i32,
+                                       _i32p, _i32p]),
+    "fanout_copy_pages": (ctypes.c_int, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _vp]),
     "fanout_extend": (ctypes.c_int, [_i32p, _i32, _i32, _i32, _i32p, _i32p, _i32, _i32p, _i32,
                                      _i32p]),
     "fanout_kv_append": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _i32, _i32p, _i32p, _i32, _i32,
@@ -107,6 +110,28 @@ def fork(prefix_pages, suffix_lens, page_size: int, free_pages, max_pages: int) 
                               _ptr(fr), int(fr.shape[0]), _ptr(table), int(max_pages)),
            "fanout_fork")
     return table[:nb]
+
+
+def fork_cow(prefix_pages, prefix_len: int, suffix_lens, page_size: int, free_pages,
+             max_pages: int):
+    """Fork with a prefix that may end inside a page: (tables, cow_pairs [B, 2], used)."""
+    pre, sl, fr = _i32arr(prefix_pages), _i32arr(suffix_lens), _i32arr(free_pages)
+    nb = int(sl.shape[0])
+    table = np.full((max(nb, 1), int(max_pages)), -1, dtype=np.int32)
+    pairs = np.full((max(nb, 1), 2), -1, dtype=np.int32)
+    used = ctypes.c_int32(0)
+    _check(load().fanout_fork_cow(_ptr(pre), int(prefix_len), nb, _ptr(sl), int(page_size),
+                                  _ptr(fr), int(fr.shape[0]), _ptr(table), int(max_pages),
+                                  _ptr(pairs), ctypes.byref(used)), "fanout_fork_cow")
+    return table[:nb], pairs[:nb], int(used.value)
+
+
+def copy_pages(k_pages, v_pages, pairs, rows: int, stream=None) -> None:
+    """Device copy of token slots [0, rows) for page pairs (int32 [n, 2] on the device)."""
+    n, h_kv, page, d = (int(x) for x in k_pages.shape)
+    _check(load().fanout_copy_pages(k_pages.data_ptr(), v_pages.data_ptr(), pairs.data_ptr(),
+                                    int(pairs.shape[0]), int(rows), n, h_kv, d, page,
+                                    _stream_handle(stream)), "fanout_copy_pages")
 
 
 def extend(page_table, prefix_len: int, suffix_lens, add_lens, page_size: int, free_pages):

@@ -104,6 +104,65 @@ int fanout_fork(const int32_t* prefix_pages, int32_t n_prefix_pages, int32_t num
     return FANOUT_OK;
 }
 
+int fanout_fork_cow(const int32_t* prefix_pages, int32_t prefix_len, int32_t num_branches,
+                    const int32_t* suffix_lens, int32_t page_size, const int32_t* free_pages,
+                    int32_t n_free, int32_t* page_table, int32_t max_pages_per_branch,
+                    int32_t* cow_pairs, int32_t* n_used) {
+    if (prefix_len < 0 || num_branches < 0 || page_size <= 0 || n_free < 0 ||
+        max_pages_per_branch < 0)
+        return FANOUT_EINVAL;
+    const int64_t n_full = prefix_len / page_size;
+    const bool partial = prefix_len % page_size != 0;
+    const int64_t n_prefix_pages = n_full + (partial ? 1 : 0);
+    if ((n_prefix_pages > 0 && !prefix_pages) || (num_branches > 0 && (!suffix_lens || !page_table)))
+        return FANOUT_EINVAL;
+    if (n_free > 0 && !free_pages) return FANOUT_EINVAL;
+    int64_t cursor = 0;
+    for (int32_t b = 0; b < num_branches; ++b) {  // check everything first
+        if (suffix_lens[b] < 0) return FANOUT_EINVAL;
+        const int64_t need =
+            (static_cast<int64_t>(prefix_len) + suffix_lens[b] + page_size - 1) / page_size;
+        if (std::max(need, n_prefix_pages) > max_pages_per_branch) return FANOUT_EINVAL;
+        cursor += std::max<int64_t>(need, n_prefix_pages) - n_full;
+        if (cursor > n_free) return FANOUT_EINVAL;
+    }
+    cursor = 0;
+    for (int32_t b = 0; b < num_branches; ++b) {
+        int32_t* row = page_table + static_cast<int64_t>(b) * max_pages_per_branch;
+        const int64_t need = std::max<int64_t>(
+            (static_cast<int64_t>(prefix_len) + suffix_lens[b] + page_size - 1) / page_size,
+            n_prefix_pages);
+        std::copy(prefix_pages, prefix_pages + n_full, row);  // whole pages: shared
+        for (int64_t i = n_full; i < need; ++i) row[i] = free_pages[cursor++];  // own pages
+        std::fill(row + need, row + max_pages_per_branch, -1);
+        if (partial && cow_pairs) {  // the partial prefix page is copied into the branch's own
+            cow_pairs[2 * b] = prefix_pages[n_full];
+            cow_pairs[2 * b + 1] = row[n_full];
+        }
+    }
+    if (n_used) *n_used = static_cast<int32_t>(cursor);
+    return FANOUT_OK;
+}
+
+int fanout_copy_pages(void* k_pages, void* v_pages, const int32_t* pairs, int32_t n_pairs,
+                      int32_t rows, int32_t num_pages, int32_t H_kv, int32_t d, int32_t page_size,
+                      fanout_stream_t stream) {
+    if (n_pairs < 0 || rows < 0 || rows > page_size || num_pages <= 0 || H_kv <= 0 || d <= 0 ||
+        page_size <= 0)
+        return FANOUT_EINVAL;
+    if (d % 8 != 0) return FANOUT_EUNSUPPORTED;
+    if (n_pairs == 0 || rows == 0) return FANOUT_OK;
+    if (!k_pages || !v_pages || !pairs) return FANOUT_EINVAL;
+    if (!ok_align16(k_pages) || !ok_align16(v_pages) || (reinterpret_cast<uintptr_t>(pairs) & 7u))
+        return FANOUT_EINVAL;
+    int32_t* err = nullptr;
+    cudaError_t ce = err_word_ptr(&err);
+    if (ce != cudaSuccess) return status_from_cuda(ce);
+    return status_from_cuda(launch_copy_pages(k_pages, v_pages, pairs, n_pairs, rows, H_kv, d,
+                                              page_size, num_pages, err,
+                                              reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int fanout_extend(int32_t* page_table, int32_t num_branches, int32_t max_pages_per_branch,
                   int32_t prefix_len, const int32_t* suffix_lens, const int32_t* add_lens,
                   int32_t page_size, const int32_t* free_pages, int32_t n_free, int32_t* n_used) {

@@ -147,6 +147,9 @@ cudaError_t launch_split_attn(const SplitParams& p, const CUtensorMap& tm_q,
                               cudaStream_t stream);
 cudaError_t launch_lse_merge(const MergeParams& p, cudaStream_t stream);
 cudaError_t err_word_ptr(int32_t** ptr);
+cudaError_t launch_copy_pages(void* k_pool, void* v_pool, const int32_t* pairs, int32_t n_pairs,
+                              int32_t rows, int32_t H_kv, int32_t d, int32_t page_size,
+                              int32_t num_pages, int32_t* err, cudaStream_t stream);
 cudaError_t launch_kv_append(const void* k_new, const void* v_new, void* k_pool, void* v_pool,
                              const int32_t* page_table, const AppendParams& p, int32_t* err,
                              cudaStream_t stream);

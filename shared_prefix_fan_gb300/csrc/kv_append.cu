@@ -11,6 +11,9 @@
 // prefix_len + suffix_len_b + t of branch b, i.e. to page
 // page_table[b][pos / page], slot pos % page, for every KV head.
 //
+// Also the copy-on-write of a partially filled shared page (fork with a
+// prefix that ends inside a page): each branch gets its own copy.
+//
 // HBM-bound scatter: one warp per (row, KV head) moves the K row with lanes
 // 0..15 and the V row with lanes 16..31 in 16-byte pieces. The per-branch
 // offsets travel in the kernel parameters, so the call needs no workspace.
@@ -59,7 +62,49 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+// Copy-on-write of partially filled pages: for every pair i, token slots
+// [0, rows) of page src[i] -> page dst[i], all KV heads, K and V.
+__global__ void __launch_bounds__(256)
+    copy_pages_kernel(uint4* __restrict__ k_pool, uint4* __restrict__ v_pool,
+                      const int2* __restrict__ pairs, int32_t n_pairs, int32_t rows, int32_t H_kv,
+                      int32_t d, int32_t page_size, int32_t num_pages, int32_t* err) {
+    const int lane = threadIdx.x & 31;
+    const int chunks = d / 8;
+    const int64_t n_items = static_cast<int64_t>(n_pairs) * H_kv * rows;
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    for (int64_t item = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+         item < n_items; item += warps) {
+        const int32_t slot = static_cast<int32_t>(item % rows);
+        const int32_t h = static_cast<int32_t>((item / rows) % H_kv);
+        const int2 pr = pairs[item / (static_cast<int64_t>(rows) * H_kv)];
+        if (pr.x < 0 || pr.x >= num_pages || pr.y < 0 || pr.y >= num_pages) {
+            if (lane == 0) atomicCAS(err, 0, 1);
+            continue;
+        }
+        const int64_t src = ((static_cast<int64_t>(pr.x) * H_kv + h) * page_size + slot) * chunks;
+        const int64_t dst = ((static_cast<int64_t>(pr.y) * H_kv + h) * page_size + slot) * chunks;
+        uint4* pool = lane >= 16 ? v_pool : k_pool;
+        for (int c = lane & 15; c < chunks; c += 16) pool[dst + c] = pool[src + c];
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_copy_pages(void* k_pool, void* v_pool, const int32_t* pairs, int32_t n_pairs,
+                              int32_t rows, int32_t H_kv, int32_t d, int32_t page_size,
+                              int32_t num_pages, int32_t* err, cudaStream_t stream) {
+    const int64_t items = static_cast<int64_t>(n_pairs) * H_kv * rows;
+    if (items <= 0) return cudaSuccess;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t blocks = (items + 7) / 8;
+    const int grid = static_cast<int>(blocks < 8LL * sms ? blocks : 8LL * sms);
+    copy_pages_kernel<<<grid, 256, 0, stream>>>(
+        static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool),
+        reinterpret_cast<const int2*>(pairs), n_pairs, rows, H_kv, d, page_size, num_pages, err);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_kv_append(const void* k_new, const void* v_new, void* k_pool, void* v_pool,
                              const int32_t* page_table, const AppendParams& p, int32_t* err,

@@ -163,7 +163,14 @@ void make_streamk(const std::vector<Range>& ranges, int32_t max_cta, Cand& c) {
 int build_plan(const PlanInput& in, Plan& plan) {
     plan = Plan();
     const int32_t B = in.num_branches;
-    const int32_t P = in.prefix_len;
+    // A prefix that ends inside a page: the whole pages are the shared range;
+    // the tail of the last prefix page is read through each branch's own table
+    // entry like its private keys (after a copy-on-write fork that entry is a
+    // private copy). Positions do not change: P + S_b = P_al + (S_b + tail).
+    const int32_t tail = in.prefix_len % in.page_size;
+    const int32_t P = in.prefix_len - tail;
+    std::vector<int32_t> S_eff(B);
+    for (int32_t b = 0; b < B; ++b) S_eff[b] = in.suffix_lens[b] + tail;
     const int32_t G = in.H_q / in.H_kv;
     std::vector<int32_t> tok0(B + 1, 0);
     int active = 0;
@@ -191,7 +198,7 @@ int build_plan(const PlanInput& in, Plan& plan) {
                 ranges.push_back({h, 0, t, std::min(tpt, R - t), 0, P, kNoCausal, false});
         }
         for (int32_t b = 0; b < B; ++b) {
-            const int32_t T = in.q_rows[b], S = in.suffix_lens[b];
+            const int32_t T = in.q_rows[b], S = S_eff[b];
             for (int32_t t = tok0[b]; t < tok0[b + 1]; t += tpt) {
                 const int32_t n = std::min(tpt, tok0[b + 1] - t);
                 const int32_t lo = shared ? P : 0;
@@ -236,7 +243,7 @@ int build_plan(const PlanInput& in, Plan& plan) {
         // when the whole KV fits in L2 (otherwise the lockstep waves of the
         // equal-chunk plan are what keeps a large shared prefix in L2).
         int64_t kv_tokens = P;
-        for (int32_t b = 0; b < B; ++b) kv_tokens += in.suffix_lens[b];
+        for (int32_t b = 0; b < B; ++b) kv_tokens += S_eff[b];
         const int64_t kv_bytes = kv_tokens * in.H_kv * kHD * 2 * 2;
         if (kv_bytes <= (100LL << 20)) {
             make_streamk(ranges, max_cta, cand);

@@ -79,7 +79,6 @@ int validate_shape(const int32_t* suffix_lens, const int32_t* q_rows, int32_t B,
     if (page_size != 16 && page_size != 32 && page_size != 64 && page_size != 128)
         return FANOUT_EUNSUPPORTED;
     if (H_q / H_kv > kBM) return FANOUT_EUNSUPPORTED;
-    if (P % page_size != 0) return FANOUT_EUNSUPPORTED;
     int64_t R = 0;
     for (int32_t b = 0; b < B; ++b) {
         const int32_t S = suffix_lens[b], T = q_rows[b];

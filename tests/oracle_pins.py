@@ -361,6 +361,43 @@ def pin_append(lib, seed=9):
         _close(lse, bl, 1e-12)
 
 
+def pin_partial_prefix(lib, seed=10):
+    """A prefix ending inside a page: fork with copy-on-write of the partial
+    page, copy it, then every branch reads back its own logical sequence
+    through its table (a gather written here) and attention equals brute force
+    ("AHBM Agentic Runtime Architecture" section 3.1: shared pages referenced,
+    the partial one copied so branches can extend it)."""
+    rng = np.random.default_rng(seed)
+    for (P, S, T, page) in ((21, [6, 0, 13], [2, 0, 5], 8), (3, [9, 4], [9, 1], 4)):
+        pb = Problem(rng, len(S), P, S, T, 8, 2, 16, page, True)
+        n_pre = -(-P // page)
+        pre_ids = np.arange(500, 500 + n_pre, dtype=np.int32)
+        free = rng.permutation(np.arange(1000, 1100, dtype=np.int32))
+        mp = n_pre + max(-(-(P + s) // page) for s in S) + 1
+        table, cow, used = oracle.fork_cow(pre_ids, P, S, page, free, mp, lib=lib)
+        assert (table[:, :P // page] == pre_ids[None, :P // page]).all()
+        assert len(np.unique(table[table >= 1000])) == (table >= 1000).sum()
+        kp = np.zeros((1100, pb.h_kv, page, pb.d), np.uint16)
+        vp = np.zeros_like(kp)
+        for j in range(P):  # the shared prefix, in the shared pages
+            kp[pre_ids[j // page], :, j % page] = pb.k_log[0][j]
+            vp[pre_ids[j // page], :, j % page] = pb.v_log[0][j]
+        kp, vp = oracle.copy_pages(kp, vp, cow, P % page, lib=lib)
+        for b in range(pb.B):  # each branch's suffix, in its own pages
+            for j in range(P, P + S[b]):
+                kp[table[b, j // page], :, j % page] = pb.k_log[b][j]
+                vp[table[b, j // page], :, j % page] = pb.v_log[b][j]
+        for b in range(pb.B):
+            for j in range(P + S[b]):
+                assert (kp[table[b, j // page], :, j % page] == pb.k_log[b][j]).all(), (b, j)
+        out, lse = oracle.attn(pb.q, kp, vp, table, P, S, T, pb.h_q, pb.h_kv, page, pb.scale,
+                               True, lib=lib)
+        bo, bl = pb.brute()
+        _close(out, bo, 1e-12)
+        _close(lse, bl, 1e-12)
+
+
 ALL_PINS = [pin_brute_force, pin_identical_keys, pin_single_key, pin_batching_invariance,
             pin_merge_invariance, pin_gqa_invariance, pin_fork_invariance,
-            pin_causal_reductions, pin_fork, pin_work_identity, pin_append]
+            pin_causal_reductions, pin_fork, pin_work_identity, pin_append,
+            pin_partial_prefix]

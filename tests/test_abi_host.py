@@ -64,7 +64,7 @@ def test_attn_rejects_bad_arguments_on_host(lib):
     E, U = binding.EINVAL, binding.EUNSUPPORTED
     assert _attn_rc(lib, d=64) == U
     assert _attn_rc(lib, ps=24) == U
-    assert _attn_rc(lib, P=40) == U            # prefix not a whole number of pages
+    assert _attn_rc(lib, P=40) not in (E, U)   # a prefix ending inside a page is accepted
     assert _attn_rc(lib, hq=6, hkv=4) == E     # H_q not a multiple of H_kv
     assert _attn_rc(lib, hq=256, hkv=1) == U   # G > 128
     assert _attn_rc(lib, T=[40, 2]) == E       # causal: more new tokens than suffix

@@ -57,3 +57,22 @@ def test_kv_append_rejects_bad_arguments_on_host():
     assert rc(mp=1) == binding.EINVAL          # rows too narrow for the grown suffix
     assert rc(k=None) == binding.EINVAL
     assert rc(kp=1032 + 2) == binding.EINVAL   # not 16-byte aligned
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_fork_cow_matches_oracle(seed):
+    rng = np.random.default_rng(100 + seed)
+    B = int(rng.integers(1, 6))
+    ps = int(rng.choice([16, 32, 64]))
+    P = int(rng.integers(0, 5 * ps))
+    S = rng.integers(0, 150, size=B)
+    n_pre = -(-P // ps)
+    ids = rng.permutation(5000).astype(np.int32)
+    mp = max(n_pre, max(-(-(P + int(s)) // ps) for s in S)) + int(rng.integers(0, 3))
+    got_t, got_c, got_u = binding.fork_cow(ids[:n_pre], P, S, ps, ids[n_pre:], mp)
+    ref_t, ref_c, ref_u = oracle.fork_cow(ids[:n_pre], P, S, ps, ids[n_pre:], mp)
+    assert np.array_equal(got_t, ref_t) and got_u == ref_u
+    if P % ps:
+        assert np.array_equal(got_c, ref_c)
+    else:  # page-aligned prefix: the ordinary fork
+        assert np.array_equal(got_t, binding.fork(ids[:n_pre], S, ps, ids[n_pre:], mp))
