@@ -654,6 +654,21 @@ __global__ void __launch_bounds__(Cfg<NQ>::kThreads, 1) __maxnreg__(NQ == 2 ? 20
     // The dependent merge kernel may be scheduled now; it waits for this grid
     // to complete before reading anything.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (warp == 0 && p.cta_first[blockIdx.x] < p.cta_first[blockIdx.x + 1]) {
+        // Start HBM traffic before the set-up below: L2 prefetches for the
+        // first tiles of this CTA's first unit.
+        const Unit u = p.units[p.cta_first[blockIdx.x]];
+        const int ps = p.page_size;
+        const int n_pages = min((u.key_end - u.key_begin + ps - 1) / ps, kPrefetch * (kBN / ps));
+        const int32_t* prow = p.page_table + static_cast<int64_t>(u.branch) * p.max_pages +
+                              u.key_begin / ps;
+        if (lane < n_pages) {
+            const int page = min(max(__ldg(prow + lane), 0), p.num_pages - 1);
+            const int64_t off = (static_cast<int64_t>(page) * p.H_kv + u.kv_head) * ps * 256;
+            ptx::prefetch_l2(p.k_base + off, static_cast<uint32_t>(ps) * 256u);
+            ptx::prefetch_l2(p.v_base + off, static_cast<uint32_t>(ps) * 256u);
+        }
+    }
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
             ptx::mbar_init(sm.bar(C::BAR_FULL + s), 1);
