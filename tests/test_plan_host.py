@@ -59,8 +59,10 @@ def check_plan(S, T, P, h_q, h_kv, ps, causal, sms=148):
             # contiguous, disjoint cover of [0, vis)
             cur = 0
             for lo, hi, _ in segs:
-                assert lo == cur or hi <= lo, (r, h, segs)
-                cur = max(cur, hi)
+                if hi <= lo:
+                    continue  # a chunk entirely in this token's causal future
+                assert lo == cur, (r, h, segs)
+                cur = hi
             assert cur == vis[r], (r, h, segs, vis[r])
             ps_ = [p_ for _, _, p_ in segs]
             if -1 in ps_:
@@ -103,12 +105,14 @@ def test_plan_balance(name):
     assert mk <= 1.25 * total / (len(cta) - 1) + 40, (mk, total / (len(cta) - 1))
 
 
-@pytest.mark.parametrize("seed", range(12))
+@pytest.mark.parametrize("seed", range(16))
 def test_plan_random(seed):
     rng = np.random.default_rng(seed)
     B = int(rng.integers(1, 6))
     ps = int(rng.choice([16, 32, 64, 128]))
     P = ps * int(rng.integers(0, 12))
+    if seed % 4 == 3:  # a prefix that ends inside a page
+        P += int(rng.integers(1, ps))
     causal = bool(rng.integers(0, 2))
     T = rng.integers(0, 40, size=B)
     S = np.array([int(t) + int(rng.integers(0 if P else 1, 300)) for t in T])
