@@ -515,7 +515,9 @@ __device__ void softmax_group(const SplitParams& p, const Smem<NQ>& sm, uint32_t
             float corr = 1.f;
             if (active) {
                 const int lim_c = vis_end - kt;  // visible columns of this tile for this row
-                const bool full = lim_c >= kBN;
+                // warp-uniform: the two passes issue warp-collective TMEM loads, so
+                // every lane of a warp must take the same code path
+                const bool full = __all_sync(0xffffffffu, lim_c >= kBN);
                 // Pass 1: the row max over the tile (two 32-column chunks per wait).
                 float mx[8];
 #pragma unroll
