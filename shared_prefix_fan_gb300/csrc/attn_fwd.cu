@@ -591,10 +591,11 @@ __device__ void softmax_group(const SplitParams& p, const Smem<NQ>& sm, uint32_t
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t r[32];
+                __syncwarp();  // converged for the warp-collective TMEM load
                 ptx::tmem_ld32(lane_addr + colO + 32 * c, r);
                 ptx::tmem_ld_wait(r);
-                if (!row_valid) continue;
-                if (direct && p.out_bf16) {
+                if (!row_valid) {
+                } else if (direct && p.out_bf16) {
                     uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) +
                                                           orow * kHD + 32 * c);
 #pragma unroll
