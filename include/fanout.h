@@ -313,12 +313,6 @@ FANOUT_API int fanout_attn_noalloc(const void *q, const void *k_pages, const voi
                 int32_t d, int32_t page_size, float scale, int32_t causal, void *out,
                 int32_t out_dtype, float *lse, fanout_stream_t stream);
 
-/* Evaluates, on the device, the software 2^x the attention kernel uses for part
- * of its softmax exponentials: y[i] = 2^x[i] (dev fp32 arrays of n elements,
- * x <= 8 expected; x < -126 gives a tiny positive value). Self-test entry:
- * compares against CUDA's exp2 in the tests. */
-FANOUT_API int fanout_selftest_exp2(const float *x, float *y, int64_t n, fanout_stream_t stream);
-
 /* Frees the workspaces of every device and stream (synchronises first). */
 FANOUT_API int fanout_release(void);
 

@@ -46,7 +46,6 @@ ABI = {
     "fanout_plan": (ctypes.c_int, [_i32p, _i32p, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32p,
                                    _i32, _i32p, _i32p, _i32, _i32p, _i32p]),
     "fanout_selftest_wait_timeout": (ctypes.c_int, [_i64, _vp]),
-    "fanout_selftest_exp2": (ctypes.c_int, [_vp, _vp, _i64, _vp]),
     "fanout_release": (ctypes.c_int, []),
     "fanout_version": (ctypes.c_char_p, []),
 }
@@ -289,15 +288,6 @@ def set_profile_events(before=None, after=None) -> None:
 
 def selftest_wait_timeout(limit_ns: int = 20_000_000, stream=None) -> int:
     return int(load().fanout_selftest_wait_timeout(int(limit_ns), _stream_handle(stream)))
-
-
-def selftest_exp2(x, stream=None):
-    """The kernels' software 2^x on a CUDA fp32 tensor."""
-    import torch
-    y = torch.empty_like(x)
-    _check(load().fanout_selftest_exp2(x.data_ptr(), y.data_ptr(), x.numel(),
-                                       _stream_handle(stream)), "fanout_selftest_exp2")
-    return y
 
 
 def release() -> None:

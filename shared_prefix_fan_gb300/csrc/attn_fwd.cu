@@ -426,12 +426,9 @@ __device__ __forceinline__ float sum8(const float (&a)[8]) {
 
 // Second softmax pass over one S buffer in TMEM: exponentials, row-sum
 // partials, and P as bf16 pairs stored over the first 64 columns (chunk pair h
-// of S -> P columns 32h .. 32h+31, all already read). In fully visible tiles
-// every kPolyEvery-th pair of columns uses the software exp2 on the FMA pipe
-// and the rest the MUFU ex2, which splits the exponential work between the
-// two units; masked tiles use ex2 only (exact zeros for masked columns).
-constexpr int kPolyEvery = 4;
-
+// of S -> P columns 32h .. 32h+31, all already read). FULL: no column of the
+// tile is masked for any row of the warp (the choice is warp-uniform, since
+// the TMEM loads are warp-collective).
 template <bool FULL>
 __device__ __forceinline__ void softmax_pass2(uint32_t s_addr, int lim_c, float sl2, float m_use,
                                               float (&sm8)[8]) {
@@ -446,23 +443,13 @@ __device__ __forceinline__ void softmax_pass2(uint32_t s_addr, int lim_c, float 
 #pragma unroll
             for (int i = 0; i < 32; i += 2) {
                 const int c = 64 * h + 32 * part + i;
-                float e0, e1;
-                if (FULL) {
-                    const float y0 = fmaf(__uint_as_float(a[i]), sl2, -m_use);
-                    const float y1 = fmaf(__uint_as_float(a[i + 1]), sl2, -m_use);
-                    if (((i >> 1) % kPolyEvery) == kPolyEvery - 1) {
-                        e0 = ptx::ex2_poly(y0);
-                        e1 = ptx::ex2_poly(y1);
-                    } else {
-                        e0 = ptx::ex2(y0);
-                        e1 = ptx::ex2(y1);
-                    }
-                } else {
-                    const float x0 = (c < lim_c) ? __uint_as_float(a[i]) : -INFINITY;
-                    const float x1 = (c + 1 < lim_c) ? __uint_as_float(a[i + 1]) : -INFINITY;
-                    e0 = ptx::ex2(fmaf(x0, sl2, -m_use));
-                    e1 = ptx::ex2(fmaf(x1, sl2, -m_use));
+                float x0 = __uint_as_float(a[i]), x1 = __uint_as_float(a[i + 1]);
+                if (!FULL) {
+                    x0 = (c < lim_c) ? x0 : -INFINITY;
+                    x1 = (c + 1 < lim_c) ? x1 : -INFINITY;
                 }
+                const float e0 = ptx::ex2(fmaf(x0, sl2, -m_use));
+                const float e1 = ptx::ex2(fmaf(x1, sl2, -m_use));
                 sm8[i & 7] += e0;
                 sm8[(i + 1) & 7] += e1;
                 pk[16 * part + (i >> 1)] = ptx::pack_bf16x2(e0, e1);

@@ -430,11 +430,6 @@ int fanout_selftest_wait_timeout(int64_t limit_ns, fanout_stream_t stream) {
     return fanout_last_error(stream);
 }
 
-int fanout_selftest_exp2(const float* x, float* y, int64_t n, fanout_stream_t stream) {
-    if (n < 0 || (n > 0 && (!x || !y))) return FANOUT_EINVAL;
-    return status_from_cuda(launch_exp2_selftest(x, y, n, reinterpret_cast<cudaStream_t>(stream)));
-}
-
 int fanout_release(void) {
     std::lock_guard<std::mutex> lk(g_mu);
     int cur = 0;

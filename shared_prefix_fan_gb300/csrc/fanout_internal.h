@@ -153,7 +153,6 @@ cudaError_t launch_copy_pages(void* k_pool, void* v_pool, const int32_t* pairs, 
 cudaError_t launch_kv_append(const void* k_new, const void* v_new, void* k_pool, void* v_pool,
                              const int32_t* page_table, const AppendParams& p, int32_t* err,
                              cudaStream_t stream);
-cudaError_t launch_exp2_selftest(const float* x, float* y, int64_t n, cudaStream_t stream);
 cudaError_t launch_wait_selftest(int32_t* err, unsigned long long limit_ns, cudaStream_t stream);
 
 }  // namespace fanout

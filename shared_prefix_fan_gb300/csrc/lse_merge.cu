@@ -130,20 +130,7 @@ __global__ void wait_selftest_kernel(int32_t* err, unsigned long long limit_ns) 
     }
 }
 
-// Evaluates the kernels' software exp2 on n inputs (self-test of the polynomial).
-__global__ void exp2_selftest_kernel(const float* __restrict__ x, float* __restrict__ y,
-                                     int64_t n) {
-    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (i < n) y[i] = ptx::ex2_poly(x[i]);
-}
-
 }  // namespace
-
-cudaError_t launch_exp2_selftest(const float* x, float* y, int64_t n, cudaStream_t stream) {
-    if (n <= 0) return cudaSuccess;
-    exp2_selftest_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(x, y, n);
-    return cudaGetLastError();
-}
 
 cudaError_t launch_lse_merge(const MergeParams& p, cudaStream_t stream) {
     if (p.n_out <= 0) return cudaSuccess;

@@ -232,21 +232,6 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-// Software 2^x on the FMA pipe (relieves the MUFU unit in the softmax):
-// x = n + f with n = round(x) taken with the 1.5*2^23 shifter, f in [-1/2, 1/2];
-// 2^f by a degree-3 polynomial (coefficients from fit_exp2_poly.py, max
-// relative error 7.5e-5 on [-1/2, 1/2]); 2^n added to the exponent field.
-// Inputs below -126 give 2^-126-ish tiny values instead of 0; callers use it
-// only where every input is a real (unmasked) score.
-__device__ __forceinline__ float ex2_poly(float x) {
-    x = fmaxf(x, -126.0f);
-    const float t = x + 12582912.0f;  // 1.5 * 2^23: low mantissa bits = round(x)
-    const float f = x - (t - 12582912.0f);
-    const float p = fmaf(fmaf(fmaf(0.0551760532f, f, 0.242611498f), f, 0.693260193f), f,
-                         0.999928057f);
-    return __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
-}
-
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
