@@ -124,12 +124,14 @@ FANOUT_API int fanout_copy_pages(void *k_pages, void *v_pages, const int32_t *pa
  * fanout_extend -- grow branch page tables for new tokens (host only).
  * "AHBM Agentic Runtime Architecture" section 3.1 (private suffix pages per
  * branch); ADR-0060 section 0.5.1 precondition P3 (the cache grows before
- * attention). Branch b's private suffix grows from suffix_lens[b] to
- * suffix_lens[b] + add_lens[b] tokens; the pages it now needs beyond its
- * current ceil(suffix_lens[b] / page_size) are taken from free_pages in order
- * (branch 0 first) and written into page_table[b] after its current pages.
+ * attention). Branch b's context grows from prefix_len + suffix_lens[b] to
+ * prefix_len + suffix_lens[b] + add_lens[b] tokens; table entry i holds
+ * logical positions [i * page_size, (i + 1) * page_size). The entries it now
+ * needs beyond its current ceil((prefix_len + suffix_lens[b]) / page_size) are
+ * taken from free_pages in order (branch 0 first).
  *   page_table   host int32 [B][max_pages_per_branch], updated in place.
- *   prefix_len   multiple of page_size.
+ *   prefix_len   any value >= 0; a prefix ending inside a page must have been
+ *                forked with fanout_fork_cow (its last page is then private).
  *   n_used       out (may be NULL): free pages consumed.
  * Returns FANOUT_EINVAL (table untouched) when a row is too narrow or the
  * free list too short.

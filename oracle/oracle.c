@@ -326,23 +326,29 @@ void oracle_copy_pages(uint16_t *k_pool, uint16_t *v_pool, const int32_t *pairs,
             }
 }
 
-/* Grow branch page tables for new tokens: branch b's private suffix goes from
- * suffix_lens[b] to suffix_lens[b] + add_lens[b] tokens; the pages it now needs
- * beyond ceil(suffix_lens[b] / page) come from free_pages in order (branch 0
- * first) and are written after its current pages. Returns the number of free
- * pages used, or -1 when the free list or a table row is too short. */
+/* Grow branch page tables for new tokens: branch b's context goes from
+ * prefix_len + suffix_lens[b] to prefix_len + suffix_lens[b] + add_lens[b]
+ * tokens, logical position j living in table entry j / page ("AHBM Agentic
+ * Runtime Architecture" section 3.1: shared prefix pages, then the branch's
+ * private pages). The entries it now needs beyond its current
+ * ceil((prefix_len + suffix_lens[b]) / page) come from free_pages in order
+ * (branch 0 first). A prefix ending inside a page needs no special case: its
+ * last page is already held (privately, after copy-on-write). Returns the
+ * number of free pages used, or -1 when the free list or a table row is too
+ * short. */
 int oracle_extend(int32_t *table, int32_t num_branches, int32_t max_pages, int32_t prefix_len,
                   const int32_t *suffix_lens, const int32_t *add_lens, int32_t page_size,
                   const int32_t *free_pages, int32_t n_free) {
     int32_t used = 0;
-    int32_t n_pre = prefix_len / page_size;
     for (int32_t b = 0; b < num_branches; ++b) {
-        int32_t have = (suffix_lens[b] + page_size - 1) / page_size;
-        int32_t need = (suffix_lens[b] + add_lens[b] + page_size - 1) / page_size;
-        if (n_pre + need > max_pages) return -1;
-        for (int32_t i = have; i < need; ++i) {
+        int64_t len0 = (int64_t)prefix_len + suffix_lens[b];
+        int64_t len1 = len0 + add_lens[b];
+        int64_t have = (len0 + page_size - 1) / page_size;
+        int64_t need = (len1 + page_size - 1) / page_size;
+        if (need > max_pages) return -1;
+        for (int64_t i = have; i < need; ++i) {
             if (used >= n_free) return -1;
-            table[(int64_t)b * max_pages + n_pre + i] = free_pages[used++];
+            table[(int64_t)b * max_pages + i] = free_pages[used++];
         }
     }
     return used;

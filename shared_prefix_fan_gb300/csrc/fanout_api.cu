@@ -167,27 +167,30 @@ int fanout_extend(int32_t* page_table, int32_t num_branches, int32_t max_pages_p
                   int32_t prefix_len, const int32_t* suffix_lens, const int32_t* add_lens,
                   int32_t page_size, const int32_t* free_pages, int32_t n_free, int32_t* n_used) {
     if (num_branches < 0 || max_pages_per_branch < 0 || prefix_len < 0 || page_size <= 0 ||
-        n_free < 0 || prefix_len % page_size != 0)
+        n_free < 0)
         return FANOUT_EINVAL;
     if (num_branches > 0 && (!page_table || !suffix_lens || !add_lens)) return FANOUT_EINVAL;
     if (n_free > 0 && !free_pages) return FANOUT_EINVAL;
-    const int64_t n_pre = prefix_len / page_size;
+    // Table entry i of a branch holds logical positions [i * page_size, (i+1) * page_size),
+    // wherever the prefix ends: held = ceil(tokens / page_size) entries.
+    auto entries = [&](int32_t b, bool grown) {
+        const int64_t tokens = static_cast<int64_t>(prefix_len) + suffix_lens[b] +
+                               (grown ? add_lens[b] : 0);
+        return (tokens + page_size - 1) / page_size;
+    };
     int64_t used = 0;
     for (int32_t b = 0; b < num_branches; ++b) {
         if (suffix_lens[b] < 0 || add_lens[b] < 0) return FANOUT_EINVAL;
-        const int64_t have = (static_cast<int64_t>(suffix_lens[b]) + page_size - 1) / page_size;
-        const int64_t need =
-            (static_cast<int64_t>(suffix_lens[b]) + add_lens[b] + page_size - 1) / page_size;
-        if (n_pre + need > max_pages_per_branch) return FANOUT_EINVAL;
-        if (used + (need - have) > n_free) return FANOUT_EINVAL;
+        const int64_t need = entries(b, true);
+        if (need > max_pages_per_branch) return FANOUT_EINVAL;
+        used += need - entries(b, false);
+        if (used > n_free) return FANOUT_EINVAL;
     }
+    used = 0;
     for (int32_t b = 0; b < num_branches; ++b) {  // checked first: no partial update on error
-        const int64_t have = (static_cast<int64_t>(suffix_lens[b]) + page_size - 1) / page_size;
-        const int64_t need =
-            (static_cast<int64_t>(suffix_lens[b]) + add_lens[b] + page_size - 1) / page_size;
-        for (int64_t i = have; i < need; ++i)
-            page_table[static_cast<int64_t>(b) * max_pages_per_branch + n_pre + i] =
-                free_pages[used++];
+        const int64_t need = entries(b, true);
+        for (int64_t i = entries(b, false); i < need; ++i)
+            page_table[static_cast<int64_t>(b) * max_pages_per_branch + i] = free_pages[used++];
     }
     if (n_used) *n_used = static_cast<int32_t>(used);
     return FANOUT_OK;

@@ -320,19 +320,26 @@ def pin_append(lib, seed=9):
     """Fork for the current suffixes, then grow the tables and append the new
     tokens' K/V: every logical key of every branch must then read back its own
     row (checked by a gather written here), and attention must match brute
-    force on the grown contexts (ADR-0060 section 0.5.1, precondition P3)."""
+    force on the grown contexts (ADR-0060 section 0.5.1, precondition P3).
+    The last case has a prefix ending inside a page (forked with copy-on-write
+    of that page): the growth continues from the branch's last token wherever
+    the prefix ended."""
     rng = np.random.default_rng(seed)
-    for (P, S_old, T, page) in (([32], [5, 16, 0], [3, 1, 4], 8), ([0], [7, 1], [2, 9], 4)):
-        P = P[0]
+    for (P, S_old, T, page) in ((32, [5, 16, 0], [3, 1, 4], 8), (0, [7, 1], [2, 9], 4),
+                                (21, [5, 0, 11], [3, 9, 1], 8)):
         S_new = [a + b for a, b in zip(S_old, T)]
         pb = Problem(rng, len(T), P, S_new, T, 8, 2, 16, page, True)
         # the state before the append: a pool holding only the old tokens
-        n_pre = P // page
-        max_pages = pb.max_pages
+        max_pages = max(-(-(P + s) // page) for s in S_new) + 1
         free = rng.permutation(np.arange(2000, 2000 + 200, dtype=np.int32))
-        table0 = oracle.fork(np.arange(1000, 1000 + n_pre, dtype=np.int32), S_old, page, free,
-                             max_pages, lib=lib)
-        n_used0 = sum((s + page - 1) // page for s in S_old)
+        n_pre = -(-P // page)
+        pre_ids = np.arange(1000, 1000 + n_pre, dtype=np.int32)
+        if P % page == 0:
+            table0 = oracle.fork(pre_ids, S_old, page, free, max_pages, lib=lib)
+            n_used0 = sum((s + page - 1) // page for s in S_old)
+        else:
+            table0, _, n_used0 = oracle.fork_cow(pre_ids, P, S_old, page, free, max_pages,
+                                                 lib=lib)
         pool_pages = 2200
         kp = np.zeros((pool_pages, pb.h_kv, page, pb.d), np.uint16)
         vp = np.zeros_like(kp)
@@ -342,8 +349,10 @@ def pin_append(lib, seed=9):
                 kp[pg, :, j % page] = pb.k_log[b][j]
                 vp[pg, :, j % page] = pb.v_log[b][j]
         table1, used = oracle.extend(table0, P, S_old, T, page, free[n_used0:], lib=lib)
-        assert used == sum((s + t + page - 1) // page - (s + page - 1) // page
+        # pages a branch holds: one per page_size of its logical positions
+        assert used == sum(-(-(P + s + t) // page) - -(-(P + s) // page)
                            for s, t in zip(S_old, T))
+        assert (table1[table0 >= 0] == table0[table0 >= 0]).all()
         grown = table1[table1 >= 0]
         assert len(np.unique(grown[grown >= 2000])) == len(grown[grown >= 2000])
         k_new = np.concatenate([pb.k_log[b][P + S_old[b]:] for b in range(pb.B)])

@@ -14,21 +14,26 @@ def _built():
     build.build()
 
 
-@pytest.mark.parametrize("seed", range(10))
+@pytest.mark.parametrize("seed", range(12))
 def test_extend_matches_oracle(seed):
+    """Odd seeds: a prefix ending inside a page, forked with copy-on-write."""
     rng = np.random.default_rng(seed)
     B = int(rng.integers(1, 7))
     ps = int(rng.choice([16, 32, 64]))
-    n_pre = int(rng.integers(0, 4))
+    P = int(rng.integers(0, 4)) * ps + (int(rng.integers(1, ps)) if seed % 2 else 0)
+    n_pre = -(-P // ps)
     S = rng.integers(0, 150, size=B)
     T = rng.integers(0, 90, size=B)
     ids = rng.permutation(4000).astype(np.int32)
-    mp = n_pre + int(max((s + t + ps - 1) // ps for s, t in zip(S, T))) + int(rng.integers(0, 3))
-    n_old = sum((int(s) + ps - 1) // ps for s in S)
-    table = binding.fork(ids[:n_pre], S, ps, ids[n_pre:], mp)
+    mp = int(max(-(-(P + s + t) // ps) for s, t in zip(S, T))) + int(rng.integers(0, 3))
+    if P % ps:
+        table, _, n_old = binding.fork_cow(ids[:n_pre], P, S, ps, ids[n_pre:], mp)
+    else:
+        n_old = sum((int(s) + ps - 1) // ps for s in S)
+        table = binding.fork(ids[:n_pre], S, ps, ids[n_pre:], mp)
     free = ids[n_pre + n_old:]
-    got, used = binding.extend(table, n_pre * ps, S, T, ps, free)
-    ref, used_ref = oracle.extend(table, n_pre * ps, S, T, ps, free)
+    got, used = binding.extend(table, P, S, T, ps, free)
+    ref, used_ref = oracle.extend(table, P, S, T, ps, free)
     assert np.array_equal(got, ref) and used == used_ref
 
 

@@ -32,8 +32,8 @@ MUTATIONS = [
      "int32_t j = prefix_len + suffix_lens[b] + t + 1;"),
     ("cow_copy_skipped", "if (partial) {\n            cow[2 * b] = prefix_pages[n_full];",
      "if (0) {\n            cow[2 * b] = prefix_pages[n_full];"),
-    ("extend_floor_pages", "int32_t have = (suffix_lens[b] + page_size - 1) / page_size;",
-     "int32_t have = suffix_lens[b] / page_size;"),
+    ("extend_floor_pages", "int64_t have = (len0 + page_size - 1) / page_size;",
+     "int64_t have = len0 / page_size;"),
 ]
 
 
