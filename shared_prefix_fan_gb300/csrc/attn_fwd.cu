@@ -55,7 +55,6 @@ constexpr int kTileBytes = kBN * kHD * 2;   // one K or V tile, bf16
 constexpr int kHalfBytes = kTileBytes / 2;  // 128 rows x 64 columns (128 B rows)
 constexpr int kQBytes = kBM * kHD * 2;
 constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold (base-2 units)
-constexpr int kPrefetch = 4;          // L2 prefetch distance in K/V tiles (x pages/tile <= 32)
 constexpr int kErrTimeout = 5;        // FANOUT_ETIMEOUT
 
 template <int NQ>
@@ -188,27 +187,6 @@ __device__ void producer_warp(const SplitParams& p, const Smem<NQ>& sm, const CU
                 win_nxt = load_window(win + 1);
             }
             const int pg_off = rel & 31;
-            {
-                // Pull the pages of the tile kPrefetch ahead into L2 now, so its TMA
-                // loads (issued once a ring stage frees up) hit L2.
-                const int jp = j + kPrefetch;
-                if (jp < n_tiles) {
-                    const int relp = jp * ppt;
-                    const int srcv = ((relp >> 5) == win) ? win_cur : win_nxt;
-                    const int n_pgp = (min(kBN, u.key_end - (u.key_begin + jp * kBN)) + ps - 1) / ps;
-                    for (int pg = 0; pg < n_pgp; ++pg) {
-                        // (clamped: an out-of-range id must not become an address)
-                        const int page = min(max(__shfl_sync(0xffffffffu, srcv, (relp & 31) + pg), 0),
-                                             p.num_pages - 1);
-                        if (lane == 0) {
-                            const int64_t off =
-                                (static_cast<int64_t>(page) * p.H_kv + u.kv_head) * ps * 256;
-                            ptx::prefetch_l2(p.k_base + off, static_cast<uint32_t>(ps) * 256u);
-                            ptx::prefetch_l2(p.v_base + off, static_cast<uint32_t>(ps) * 256u);
-                        }
-                    }
-                }
-            }
             for (int kv = 0; kv < 2 && ok; ++kv, ++it) {
                 const uint32_t stage = it % C::kStages;
                 const uint32_t par = (it / C::kStages) & 1u;
@@ -424,41 +402,6 @@ __device__ __forceinline__ float sum8(const float (&a)[8]) {
     return ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
 }
 
-// Second softmax pass over one S buffer in TMEM: exponentials, row-sum
-// partials, and P as bf16 pairs stored over the first 64 columns (chunk pair h
-// of S -> P columns 32h .. 32h+31, all already read). FULL: no column of the
-// tile is masked for any row of the warp (the choice is warp-uniform, since
-// the TMEM loads are warp-collective).
-template <bool FULL>
-__device__ __forceinline__ void softmax_pass2(uint32_t s_addr, int lim_c, float sl2, float m_use,
-                                              float (&sm8)[8]) {
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int part = 0; part < 2; ++part) {
-            uint32_t a[32];
-            ptx::tmem_ld32(s_addr + 64 * h + 32 * part, a);
-            ptx::tmem_ld_wait(a);
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-                const int c = 64 * h + 32 * part + i;
-                float x0 = __uint_as_float(a[i]), x1 = __uint_as_float(a[i + 1]);
-                if (!FULL) {
-                    x0 = (c < lim_c) ? x0 : -INFINITY;
-                    x1 = (c + 1 < lim_c) ? x1 : -INFINITY;
-                }
-                const float e0 = ptx::ex2(fmaf(x0, sl2, -m_use));
-                const float e1 = ptx::ex2(fmaf(x1, sl2, -m_use));
-                sm8[i & 7] += e0;
-                sm8[(i + 1) & 7] += e1;
-                pk[16 * part + (i >> 1)] = ptx::pack_bf16x2(e0, e1);
-            }
-        }
-        ptx::tmem_st32(s_addr + 32 * h, pk);
-    }
-}
-
 // Group x owns query tile x of every unit (rows 128x .. 128x+127); thread i
 // owns row i of the tile (TMEM lane i). A warp whose 32 rows are all padding
 // follows the barrier protocol but skips the TMEM traffic and the math.
@@ -501,44 +444,51 @@ __device__ void softmax_group(const SplitParams& p, const Smem<NQ>& sm, uint32_t
             const uint32_t colS = s_col<NQ>(x, jt);
             float corr = 1.f;
             if (active) {
-                const int lim_c = vis_end - kt;  // visible columns of this tile for this row
-                // warp-uniform: the two passes issue warp-collective TMEM loads, so
-                // every lane of a warp must take the same code path
+                const int lim_c = vis_end - kt;
                 const bool full = __all_sync(0xffffffffu, lim_c >= kBN);
-                // Pass 1: the row max over the tile (two 32-column chunks per wait).
+                uint32_t s[kBN];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t (&chunk)[32] = *reinterpret_cast<uint32_t (*)[32]>(&s[32 * c]);
+                    ptx::tmem_ld32(lane_addr + colS + 32 * c, chunk);
+                }
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t (&chunk)[32] = *reinterpret_cast<uint32_t (*)[32]>(&s[32 * c]);
+                    if (c == 0) ptx::tmem_ld_wait(chunk); else ptx::reg_touch(chunk);
+                }
+                if (!full) {
+#pragma unroll
+                    for (int c = 0; c < kBN; ++c)
+                        if (c >= lim_c) s[c] = __float_as_uint(-INFINITY);
+                }
                 float mx[8];
 #pragma unroll
                 for (int q = 0; q < 8; ++q) mx[q] = -INFINITY;
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t a[32], b[32];
-                    ptx::tmem_ld32(lane_addr + colS + 64 * h, a);
-                    ptx::tmem_ld32(lane_addr + colS + 64 * h + 32, b);
-                    ptx::tmem_ld_wait(a);
-                    ptx::reg_touch(b);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int c0 = 64 * h + i, c1 = c0 + 32;
-                        const float v0 = (full || c0 < lim_c) ? __uint_as_float(a[i]) : -INFINITY;
-                        const float v1 = (full || c1 < lim_c) ? __uint_as_float(b[i]) : -INFINITY;
-                        mx[i & 7] = fmaxf(mx[i & 7], fmaxf(v0, v1));
-                    }
-                }
+                for (int c = 0; c < kBN; ++c) mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(s[c]));
                 const float mt = max8(mx) * sl2;  // scale > 0: max commutes with scaling
                 if (mt > m_ref + kRescaleLog2) {
                     corr = (m_ref == -INFINITY) ? 0.f : ptx::ex2(m_ref - mt);
                     m_ref = mt;
                 }
                 const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-                // Pass 2: P = 2^(S*scale*log2e - m), row sum, bf16 pairs written over
-                // S columns this pass has already read (chunk pair h -> P columns 32h..).
                 float sm8[8];
 #pragma unroll
                 for (int q = 0; q < 8; ++q) sm8[q] = 0.f;
-                if (full) {
-                    softmax_pass2<true>(lane_addr + colS, 0, sl2, m_use, sm8);
-                } else {
-                    softmax_pass2<false>(lane_addr + colS, lim_c, sl2, m_use, sm8);
+#pragma unroll
+                for (int c = 0; c < kBN; ++c) {
+                    const float e = ptx::ex2(fmaf(__uint_as_float(s[c]), sl2, -m_use));
+                    s[c] = __float_as_uint(e);
+                    sm8[c & 7] += e;
+                }
+#pragma unroll
+                for (int i = 0; i < 64; ++i)
+                    s[i] = ptx::pack_bf16x2(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1]));
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t (&chunk)[32] = *reinterpret_cast<uint32_t (*)[32]>(&s[32 * c]);
+                    ptx::tmem_st32(lane_addr + colS + 32 * c, chunk);
                 }
                 l_run = l_run * corr + sum8(sm8);
                 ptx::tmem_st_wait();
@@ -644,21 +594,6 @@ __global__ void __launch_bounds__(Cfg<NQ>::kThreads, 1) __maxnreg__(NQ == 2 ? 20
     // The dependent merge kernel may be scheduled now; it waits for this grid
     // to complete before reading anything.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    if (warp == 0 && p.cta_first[blockIdx.x] < p.cta_first[blockIdx.x + 1]) {
-        // Start HBM traffic before the set-up below: L2 prefetches for the
-        // first tiles of this CTA's first unit.
-        const Unit u = p.units[p.cta_first[blockIdx.x]];
-        const int ps = p.page_size;
-        const int n_pages = min((u.key_end - u.key_begin + ps - 1) / ps, kPrefetch * (kBN / ps));
-        const int32_t* prow = p.page_table + static_cast<int64_t>(u.branch) * p.max_pages +
-                              u.key_begin / ps;
-        if (lane < n_pages) {
-            const int page = min(max(__ldg(prow + lane), 0), p.num_pages - 1);
-            const int64_t off = (static_cast<int64_t>(page) * p.H_kv + u.kv_head) * ps * 256;
-            ptx::prefetch_l2(p.k_base + off, static_cast<uint32_t>(ps) * 256u);
-            ptx::prefetch_l2(p.v_base + off, static_cast<uint32_t>(ps) * 256u);
-        }
-    }
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
             ptx::mbar_init(sm.bar(C::BAR_FULL + s), 1);

@@ -64,8 +64,6 @@ int build_plan(const PlanInput& in, Plan& plan);
 
 struct SplitParams {
     const int32_t* page_table;
-    const uint8_t* k_base;  // page pools (for L2 prefetches ahead of the TMA loads)
-    const uint8_t* v_base;
     const Unit* units;
     const int32_t* cta_first;
     float* part_o;    // [part][128 * nq rows][kHD]

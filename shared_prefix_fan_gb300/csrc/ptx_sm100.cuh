@@ -89,12 +89,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, 
         : "memory");
 }
 
-// Bulk prefetch of [addr, addr + bytes) into L2 (no shared memory involved).
-__device__ __forceinline__ void prefetch_l2(const void* addr, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(addr)),
-                 "r"(bytes)
-                 : "memory");
-}
 
 // ----------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {

@@ -159,8 +159,6 @@ int launch_plan(const CallArgs& a, const Plan& pl, const Layout& L, uint8_t* bas
 
     SplitParams p;
     p.page_table = a.page_table;
-    p.k_base = static_cast<const uint8_t*>(a.k);
-    p.v_base = static_cast<const uint8_t*>(a.v);
     p.units = reinterpret_cast<const Unit*>(base + L.units);
     p.cta_first = reinterpret_cast<const int32_t*>(base + L.cta);
     p.part_o = reinterpret_cast<float*>(base + L.o);
