@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_HERE, "lib", "libfanout.so")
 
 OK, EINVAL, EUNSUPPORTED, ECUDA, ENOMEM, ETIMEOUT = range(6)
 OUT_F32, OUT_BF16 = 0, 1
-OPT_SPLITS, OPT_VALIDATE_TABLE, OPT_WAIT_LIMIT_NS, OPT_NUM_SMS = 1, 2, 3, 4
+OPT_SPLITS, OPT_VALIDATE_TABLE, OPT_WAIT_LIMIT_NS, OPT_NUM_SMS, OPT_FUSED_MERGE = 1, 2, 3, 4, 5
 
 # The C ABI (include/fanout.h): name -> (restype, argtypes)
 _i32, _i64, _f32, _vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p

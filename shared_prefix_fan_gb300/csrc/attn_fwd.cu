@@ -46,6 +46,7 @@
 #include <cuda_bf16.h>
 
 #include "fanout_internal.h"
+#include "merge_row.cuh"
 #include "ptx_sm100.cuh"
 
 namespace fanout {
@@ -102,6 +103,9 @@ struct Smem {
     __device__ uint32_t* tmem_slot() const { return reinterpret_cast<uint32_t*>(ptr + C::kSmemMisc); }
     __device__ volatile int* abort_flag() const {
         return reinterpret_cast<volatile int*>(ptr + C::kSmemMisc + 4);
+    }
+    __device__ volatile int* merge_go() const {
+        return reinterpret_cast<volatile int*>(ptr + C::kSmemMisc + 8);
     }
 };
 
@@ -574,6 +578,60 @@ __device__ void softmax_group(const SplitParams& p, const Smem<NQ>& sm, uint32_t
     }
 }
 
+// ------------------------------------------------------------------ merge tail
+// The log-sum-exp merge of the split-KV partials inside this grid (launched
+// cooperatively, so every CTA is resident): each CTA publishes the call's
+// epoch once its partials are written, waits (bounded) until every CTA has,
+// then merges its slice of the output rows, one warp per row. This replaces
+// the separate merge launch; the per-row arithmetic is merge_row's.
+template <int NQ>
+__device__ void merge_tail(const SplitParams& p, const Smem<NQ>& sm) {
+    using C = Cfg<NQ>;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    // The __syncthreads before this call orders every partial store of the CTA
+    // before thread 0's fence and release.
+    if (threadIdx.x == 0) {
+        __threadfence();
+        ptx::st_release_gpu(p.flags + blockIdx.x, p.epoch);
+    }
+    if (warp == 0) {
+        bool all = false;
+        const uint64_t t0 = ptx::globaltimer_ns();
+        for (;;) {
+            bool mine = true;
+            for (int c = lane; c < static_cast<int>(gridDim.x); c += 32)
+                mine = mine && ptx::ld_acquire_gpu(p.flags + c) == p.epoch;
+            if (__all_sync(0xffffffffu, mine)) {
+                all = true;
+                break;
+            }
+            if (ptx::globaltimer_ns() - t0 > p.wait_limit_ns) break;
+            __nanosleep(64);
+        }
+        __threadfence();  // every lane: its acquires before the CTA's reads below
+        if (lane == 0) {
+            if (!all && atomicCAS(p.err, 0, kErrTimeout) == 0) {
+                p.err[1] = 30;
+                p.err[2] = static_cast<int32_t>(blockIdx.x);
+            }
+            *sm.merge_go() = all ? 1 : 0;
+        }
+    }
+    __syncthreads();
+    if (!*sm.merge_go()) return;
+    const int64_t n_out = p.merge.n_out;
+    const int64_t per = (n_out + gridDim.x - 1) / gridDim.x;
+    const int64_t r0 = static_cast<int64_t>(blockIdx.x) * per;
+    const int64_t r1 = min(n_out, r0 + per);
+    constexpr int kWarps = C::kThreads / 32;
+    if (p.merge.merge_stride <= 8) {
+        for (int64_t n = r0 + warp; n < r1; n += kWarps) merge_row<8>(p.merge, n, lane);
+    } else {
+        for (int64_t n = r0 + warp; n < r1; n += kWarps) merge_row<24>(p.merge, n, lane);
+    }
+}
+
 template <int NQ>
 __global__ void __launch_bounds__(Cfg<NQ>::kThreads, 1) __maxnreg__(NQ == 2 ? 200 : 255)
     attn_fwd_kernel(const __grid_constant__ SplitParams p,
@@ -643,11 +701,12 @@ __global__ void __launch_bounds__(Cfg<NQ>::kThreads, 1) __maxnreg__(NQ == 2 ? 20
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, C::kTmemCols);
     }
+    if (p.fused_merge) merge_tail<NQ>(p, sm);
 }
 
 template <int NQ>
 cudaError_t launch_nq(const SplitParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
-                      const CUtensorMap& tm_v, int grid, cudaStream_t stream) {
+                      const CUtensorMap& tm_v, int grid, bool cooperative, cudaStream_t stream) {
     static bool attr_set[64] = {};  // the attribute is set once per device
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -658,18 +717,26 @@ cudaError_t launch_nq(const SplitParams& p, const CUtensorMap& tm_q, const CUten
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) attr_set[dev] = true;
     }
-    attn_fwd_kernel<NQ><<<grid, Cfg<NQ>::kThreads, Cfg<NQ>::kSmemAlloc, stream>>>(p, tm_q, tm_k,
-                                                                                 tm_v);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(Cfg<NQ>::kThreads);
+    cfg.dynamicSmemBytes = Cfg<NQ>::kSmemAlloc;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = cooperative ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, attn_fwd_kernel<NQ>, p, tm_q, tm_k, tm_v);
 }
 
 }  // namespace
 
 cudaError_t launch_split_attn(const SplitParams& p, const CUtensorMap& tm_q,
                               const CUtensorMap& tm_k, const CUtensorMap& tm_v, int grid,
-                              cudaStream_t stream) {
-    return p.nq == 2 ? launch_nq<2>(p, tm_q, tm_k, tm_v, grid, stream)
-                     : launch_nq<1>(p, tm_q, tm_k, tm_v, grid, stream);
+                              bool cooperative, cudaStream_t stream) {
+    return p.nq == 2 ? launch_nq<2>(p, tm_q, tm_k, tm_v, grid, cooperative, stream)
+                     : launch_nq<1>(p, tm_q, tm_k, tm_v, grid, cooperative, stream);
 }
 
 }  // namespace fanout

@@ -25,6 +25,7 @@ std::mutex g_mu;
 int64_t g_force_splits = 0;
 int64_t g_validate_table = 0;
 int64_t g_num_sms_override = 0;
+int64_t g_fused_merge = 1;
 unsigned long long g_wait_limit_ns = 1000000000ull;
 cudaEvent_t g_ev_before = nullptr;
 cudaEvent_t g_ev_after = nullptr;
@@ -36,6 +37,7 @@ struct Workspace {
     Plan plan;
     Layout layout{};
     bool plan_ready = false;
+    uint32_t epoch = 0;  // flag value of the last call (fused merge)
 };
 std::map<std::pair<int, cudaStream_t>, Workspace*> g_ws;
 
@@ -60,6 +62,10 @@ namespace fanout {
 int32_t current_force_splits() {
     std::lock_guard<std::mutex> lk(g_mu);
     return static_cast<int32_t>(g_force_splits);
+}
+int32_t current_fused_merge() {
+    std::lock_guard<std::mutex> lk(g_mu);
+    return static_cast<int32_t>(g_fused_merge);
 }
 }  // namespace fanout
 
@@ -255,6 +261,10 @@ int fanout_set_option(int32_t option, int64_t value) {
             g_num_sms_override = value;
             for (auto& kv : g_ws) kv.second->plan_ready = false;
             return FANOUT_OK;
+        case FANOUT_OPT_FUSED_MERGE:
+            if (value != 0 && value != 1) return FANOUT_EINVAL;
+            g_fused_merge = value;
+            return FANOUT_OK;
         default: return FANOUT_EINVAL;
     }
 }
@@ -361,14 +371,20 @@ int fanout_attn(const void* q, const void* k_pages, const void* v_pages,
                 return status_from_cuda(ce);
             }
             ws->cap = ws->layout.total;
+            // fused-merge flags start below every epoch a call can use
+            ce = cudaMemsetAsync(static_cast<uint8_t*>(ws->buf) + ws->layout.flags, 0,
+                                 kMaxFusedGrid * sizeof(uint32_t), stream);
+            if (ce != cudaSuccess) return status_from_cuda(ce);
         }
         ce = upload_plan(ws->plan, ws->layout, static_cast<uint8_t*>(ws->buf), stream);
         if (ce != cudaSuccess) return status_from_cuda(ce);
         ws->key = key;
         ws->plan_ready = true;
     }
+    if (++ws->epoch == 0) ws->epoch = 1;  // 0 is the flags' initial value
     CallArgs a{q, k_pages, v_pages, page_table, max_pages_per_branch, num_pages, H_q, H_kv,
-               page_size, out_dtype == FANOUT_OUT_BF16, scale, out, lse, R, g_wait_limit_ns};
+               page_size, out_dtype == FANOUT_OUT_BF16, scale, out, lse, R, g_wait_limit_ns,
+               static_cast<int32_t>(g_fused_merge), ws->epoch};
     return launch_plan(a, ws->plan, ws->layout, static_cast<uint8_t*>(ws->buf), stream,
                        g_ev_before, g_ev_after);
 }

@@ -62,6 +62,26 @@ struct Plan {
 // Builds the work plan (host only). Returns a fanout_status code.
 int build_plan(const PlanInput& in, Plan& plan);
 
+struct MergeParams {
+    const float* part_o;
+    const float2* part_ml;
+    const int32_t* merge_cnt;  // null: uniform parts (n_parts per output, part-major)
+    const int2* merge_ent;     // [key][stride] {part, row base}
+    int32_t merge_stride;
+    int32_t n_parts;           // uniform mode only
+    int64_t n_out;             // rows of out: R*H_q (or n for uniform mode)
+    int32_t H_q, G;            // planned mode: out row n = token*H_q + kv_head*G + g
+    int32_t rows_per_part;     // planned mode: rows of one partial block
+    void* out;
+    int32_t out_bf16;
+    float* lse;
+};
+
+// Grid flags for the merge inside the attention kernel: one epoch word per CTA
+// at the start of the plan's device scratch (so a re-laid-out plan never
+// aliases them); a grid is at most this many CTAs when the merge is fused.
+constexpr int kMaxFusedGrid = 1024;
+
 struct SplitParams {
     const int32_t* page_table;
     const Unit* units;
@@ -78,22 +98,15 @@ struct SplitParams {
     int32_t out_bf16;
     float scale_log2;  // scale * log2(e)
     unsigned long long wait_limit_ns;
+    // Merge inside the attention kernel (cooperative launch, all CTAs resident):
+    // each CTA publishes `epoch` in flags[blockIdx.x] after its partials, waits
+    // for every CTA's flag, then merges a slice of the output rows.
+    int32_t fused_merge;
+    uint32_t epoch;
+    uint32_t* flags;
+    MergeParams merge;
 };
 
-struct MergeParams {
-    const float* part_o;
-    const float2* part_ml;
-    const int32_t* merge_cnt;  // null: uniform parts (n_parts per output, part-major)
-    const int2* merge_ent;     // [key][stride] {part, row base}
-    int32_t merge_stride;
-    int32_t n_parts;           // uniform mode only
-    int64_t n_out;             // rows of out: R*H_q (or n for uniform mode)
-    int32_t H_q, G;            // planned mode: out row n = token*H_q + kv_head*G + g
-    int32_t rows_per_part;     // planned mode: rows of one partial block
-    void* out;
-    int32_t out_bf16;
-    float* lse;
-};
 
 // One call: validated arguments (host) for the shared launch path.
 struct CallArgs {
@@ -108,11 +121,13 @@ struct CallArgs {
     float* lse;
     int64_t R;
     unsigned long long wait_limit_ns;
+    int32_t fused_merge;  // 1: merge inside the attention kernel when the grid fits
+    uint32_t epoch;       // this call's flag value (never 0; distinct from the last call's)
 };
 
 // Device layout of a plan inside one scratch buffer.
 struct Layout {
-    size_t units, cta, mcnt, ment, ml, o, total;
+    size_t flags, units, cta, mcnt, ment, ml, o, total;
 };
 Layout plan_layout(const Plan& pl);
 // Copies the plan's tables into `base` (device) on `stream`.
@@ -122,6 +137,8 @@ int launch_plan(const CallArgs& a, const Plan& pl, const Layout& L, uint8_t* bas
                 cudaStream_t stream, cudaEvent_t ev_before, cudaEvent_t ev_after);
 // The FANOUT_OPT_SPLITS setting (0 = planner's choice).
 int32_t current_force_splits();
+// The FANOUT_OPT_FUSED_MERGE setting.
+int32_t current_fused_merge();
 // Host-side argument checks shared by the entry points (fanout_status code).
 int validate_shape(const int32_t* suffix_lens, const int32_t* q_rows, int32_t B, int32_t P,
                    int32_t H_q, int32_t H_kv, int32_t d, int32_t page_size, int32_t causal);
@@ -140,9 +157,10 @@ struct AppendParams {
 };
 
 // Launchers (defined in the .cu files); return cudaError_t.
+// cooperative: launch with all CTAs co-resident (required when p.fused_merge).
 cudaError_t launch_split_attn(const SplitParams& p, const CUtensorMap& tm_q,
                               const CUtensorMap& tm_k, const CUtensorMap& tm_v, int grid,
-                              cudaStream_t stream);
+                              bool cooperative, cudaStream_t stream);
 cudaError_t launch_lse_merge(const MergeParams& p, cudaStream_t stream);
 cudaError_t err_word_ptr(int32_t** ptr);
 cudaError_t launch_copy_pages(void* k_pool, void* v_pool, const int32_t* pairs, int32_t n_pairs,

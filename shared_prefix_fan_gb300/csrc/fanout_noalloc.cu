@@ -7,8 +7,8 @@
 // engine that reserves nearly all device memory up front for its own pool and
 // forbids any other allocation, code that must never trigger the device-wide
 // synchronisation cudaFree implies, and callers running where allocation is
-// not permitted at all. This entry point runs the same two kernels (split-KV
-// attention, log-sum-exp merge) with their scratch -- the work plan and the
+// not permitted at all. This entry point runs the same kernels (split-KV
+// attention with its log-sum-exp merge) with their scratch -- the work plan and the
 // split partials -- in one fixed array compiled into the library instead.
 //
 // The array. kScratchBytes (FANOUT_NOALLOC_SCRATCH_BYTES, 32 MiB) of device
@@ -21,7 +21,9 @@
 // capture). All calls share the array and it keeps the last call's contents:
 // nothing in it is read before the same call writes it (the plan is uploaded
 // every call, and every partial slot the merge reads is written by one unit
-// of the same call), so no clearing is needed. Calls that overlap on the GPU
+// of the same call) except the fused merge's per-CTA flags at its start,
+// which only ever hold 0 (the array's initial value) or an earlier call's
+// epoch, never the current one -- so no clearing is needed. Calls that overlap on the GPU
 // (different streams, or a second call before the first finished) race on the
 // array and corrupt each other's results.
 #include <cuda_runtime.h>
@@ -42,6 +44,7 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[kScratchBytes];
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mu;
 void* g_scratch_addr[kMaxDevices] = {};
+uint32_t g_epoch[kMaxDevices] = {};  // fused-merge flag value of the last call per device
 
 // Once per device, with that device current: the device address of the array.
 int scratch_for_device(int dev, uint8_t** out) {
@@ -92,7 +95,14 @@ extern "C" FANOUT_API int fanout_attn_noalloc(
     if ((st = scratch_for_device(dev, &scratch)) != FANOUT_OK) return st;
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     if (upload_plan(plan, L, scratch, stream) != cudaSuccess) return FANOUT_ECUDA;
+    uint32_t epoch;
+    {
+        std::lock_guard<std::mutex> lk(g_setup_mu);
+        if (++g_epoch[dev] == 0) g_epoch[dev] = 1;
+        epoch = g_epoch[dev];
+    }
     CallArgs a{q, k_pages, v_pages, page_table, max_pages_per_branch, num_pages, H_q, H_kv,
-               page_size, out_dtype == FANOUT_OUT_BF16, scale, out, lse, R, 1000000000ull};
+               page_size, out_dtype == FANOUT_OUT_BF16, scale, out, lse, R, 1000000000ull,
+               current_fused_merge(), epoch};
     return launch_plan(a, plan, L, scratch, stream, nullptr, nullptr);
 }

@@ -111,6 +111,8 @@ int validate_call(const void* q, const void* k, const void* v, const int32_t* pa
 Layout plan_layout(const Plan& pl) {
     Layout L;
     size_t off = 0;
+    L.flags = off;  // always first: epochs of the fused merge (zero when first allocated)
+    off = align256(off + kMaxFusedGrid * sizeof(uint32_t));
     L.units = off;
     off = align256(off + pl.units.size() * sizeof(Unit));
     L.cta = off;
@@ -178,26 +180,42 @@ int launch_plan(const CallArgs& a, const Plan& pl, const Layout& L, uint8_t* bas
     p.out_bf16 = a.out_bf16;
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.wait_limit_ns = a.wait_limit_ns;
+    MergeParams& m = p.merge;
+    m.part_o = p.part_o;
+    m.part_ml = p.part_ml;
+    m.merge_cnt = reinterpret_cast<const int32_t*>(base + L.mcnt);
+    m.merge_ent = reinterpret_cast<const int2*>(base + L.ment);
+    m.merge_stride = pl.merge_stride;
+    m.n_parts = 0;
+    m.n_out = a.R * a.H_q;
+    m.H_q = a.H_q;
+    m.G = G;
+    m.rows_per_part = kBM * pl.nq;
+    m.out = a.out;
+    m.out_bf16 = a.out_bf16;
+    m.lse = a.lse;
+    p.flags = reinterpret_cast<uint32_t*>(base + L.flags);
+    p.epoch = a.epoch;
+    // The merge runs inside the attention kernel when every CTA can be resident
+    // at once (one per SM); otherwise, or if the cooperative launch is refused,
+    // as a separate kernel.
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const bool fuse = pl.need_merge && a.fused_merge && pl.n_cta() <= kMaxFusedGrid &&
+                      pl.n_cta() <= sms;
 
     if (ev_before) cudaEventRecord(ev_before, stream);
-    ce = launch_split_attn(p, tm_q, tm_k, tm_v, pl.n_cta(), stream);
+    p.fused_merge = fuse ? 1 : 0;
+    ce = launch_split_attn(p, tm_q, tm_k, tm_v, pl.n_cta(), fuse, stream);
+    if (ce != cudaSuccess && fuse) {
+        (void)cudaGetLastError();  // refused as a cooperative launch: merge separately
+        p.fused_merge = 0;
+        ce = launch_split_attn(p, tm_q, tm_k, tm_v, pl.n_cta(), false, stream);
+    }
     if (ev_after) cudaEventRecord(ev_after, stream);
     if (ce != cudaSuccess) return status_of(ce);
-    if (pl.need_merge) {
-        MergeParams m;
-        m.part_o = p.part_o;
-        m.part_ml = p.part_ml;
-        m.merge_cnt = reinterpret_cast<const int32_t*>(base + L.mcnt);
-        m.merge_ent = reinterpret_cast<const int2*>(base + L.ment);
-        m.merge_stride = pl.merge_stride;
-        m.n_parts = 0;
-        m.n_out = a.R * a.H_q;
-        m.H_q = a.H_q;
-        m.G = G;
-        m.rows_per_part = kBM * pl.nq;
-        m.out = a.out;
-        m.out_bf16 = a.out_bf16;
-        m.lse = a.lse;
+    if (pl.need_merge && !p.fused_merge) {
         ce = launch_lse_merge(m, stream);
         if (ce != cudaSuccess) return status_of(ce);
     }

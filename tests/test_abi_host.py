@@ -44,6 +44,9 @@ def test_options_validated(lib):
     assert lib.fanout_set_option(99, 1) == binding.EINVAL
     assert lib.fanout_set_option(binding.OPT_WAIT_LIMIT_NS, 0) == binding.EINVAL
     assert lib.fanout_set_option(binding.OPT_SPLITS, 0) == binding.OK
+    assert lib.fanout_set_option(binding.OPT_FUSED_MERGE, 2) == binding.EINVAL
+    assert lib.fanout_set_option(binding.OPT_FUSED_MERGE, 0) == binding.OK
+    assert lib.fanout_set_option(binding.OPT_FUSED_MERGE, 1) == binding.OK
 
 
 def _attn_rc(lib, **kw):

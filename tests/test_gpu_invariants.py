@@ -69,6 +69,43 @@ def test_split_invariance():
     assert (l1 - l7).abs().max().item() <= 1e-4
 
 
+@pytest.mark.parametrize("name", ["decode", "batching", "tiny"])
+def test_fused_merge_equals_separate_merge(name):
+    """The merge inside the attention kernel (grid flags, cooperative launch) and
+    the separate merge kernel run the same per-row fold on the same partials:
+    bitwise equal, and both match the oracle."""
+    w = draw(WORKLOADS[name])
+    dw = DevWorkload(w)
+    try:
+        binding.set_option(binding.OPT_FUSED_MERGE, 0)
+        o_sep, l_sep = dw.run()
+        binding.set_option(binding.OPT_FUSED_MERGE, 1)
+        o_fused, l_fused = dw.run()
+        o_again, l_again = dw.run()   # next epoch on the same flags
+    finally:
+        binding.set_option(binding.OPT_FUSED_MERGE, 1)
+    assert torch.equal(o_sep, o_fused) and torch.equal(l_sep, l_fused)
+    assert torch.equal(o_fused, o_again) and torch.equal(l_fused, l_again)
+    compare(o_fused, l_fused, *oracle_ref(w), what=name + " fused merge")
+
+
+def test_grid_larger_than_device_merges_separately():
+    """A plan for more CTAs than the device holds at once cannot be launched
+    cooperatively: the separate merge kernel runs instead, same results."""
+    w = draw(WORKLOADS["decode"])
+    dw = DevWorkload(w)
+    o0, l0 = dw.run()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    try:
+        binding.set_option(binding.OPT_NUM_SMS, 2 * sms)
+        o1, l1 = dw.run()
+    finally:
+        binding.set_option(binding.OPT_NUM_SMS, 0)
+    assert binding.last_error() == binding.OK
+    assert (o1 - o0).abs().max().item() <= 1e-4
+    assert (l1 - l0).abs().max().item() <= 1e-4
+
+
 def test_single_token_causal_equals_noncausal():
     dw = DevWorkload(draw(WORKLOADS["decode"]))
     oc, lc = dw.run(causal=True)
