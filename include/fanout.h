@@ -259,7 +259,8 @@ FANOUT_API int fanout_set_option(int32_t option, int64_t value);
 
 /* Record `before` / `after` on the call's stream around the split-KV attention
  * kernel of every following fanout_attn call (NULL, NULL turns it off). Used to
- * time that kernel alone. */
+ * time that kernel alone (it includes the merge when the merge is fused, see
+ * FANOUT_OPT_FUSED_MERGE; a separate merge kernel falls outside the events). */
 FANOUT_API int fanout_set_profile_events(fanout_event_t before, fanout_event_t after);
 
 /* Host-side description of the work plan fanout_attn would run for a problem
