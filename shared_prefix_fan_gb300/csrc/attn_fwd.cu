@@ -587,6 +587,7 @@ __device__ void softmax_group(const SplitParams& p, const Smem<NQ>& sm, uint32_t
 template <int NQ>
 __device__ void merge_tail(const SplitParams& p, const Smem<NQ>& sm) {
     using C = Cfg<NQ>;
+    constexpr int kWarps = C::kThreads / 32;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     // The __syncthreads before this call orders every partial store of the CTA
@@ -595,21 +596,31 @@ __device__ void merge_tail(const SplitParams& p, const Smem<NQ>& sm) {
         __threadfence();
         ptx::st_release_gpu(p.flags + blockIdx.x, p.epoch);
     }
+    // This CTA's rows; the merge index of each warp's first row is plan data,
+    // read while the other CTAs finish.
+    const int64_t n_out = p.merge.n_out;
+    const int64_t per = (n_out + gridDim.x - 1) / gridDim.x;
+    const int64_t r0 = static_cast<int64_t>(blockIdx.x) * per;
+    const int64_t r1 = min(n_out, r0 + per);
+    const int64_t n_first = r0 + warp;
+    MergeIdx ix0{0, 0, 0, make_int2(0, 0)};
+    if (n_first < r1) ix0 = merge_index(p.merge, n_first, lane);
     if (warp == 0) {
         bool all = false;
         const uint64_t t0 = ptx::globaltimer_ns();
         for (;;) {
+            // all of this lane's flags in one round trip (relaxed loads; the
+            // fence after the loop orders the reads that depend on them)
             bool mine = true;
             for (int c = lane; c < static_cast<int>(gridDim.x); c += 32)
-                mine = mine && ptx::ld_acquire_gpu(p.flags + c) == p.epoch;
+                mine &= ptx::ld_relaxed_gpu(p.flags + c) == p.epoch;
             if (__all_sync(0xffffffffu, mine)) {
                 all = true;
                 break;
             }
             if (ptx::globaltimer_ns() - t0 > p.wait_limit_ns) break;
-            __nanosleep(64);
         }
-        __threadfence();  // every lane: its acquires before the CTA's reads below
+        __threadfence();  // every lane: acquire side of the flags it read
         if (lane == 0) {
             if (!all && atomicCAS(p.err, 0, kErrTimeout) == 0) {
                 p.err[1] = 30;
@@ -620,15 +631,12 @@ __device__ void merge_tail(const SplitParams& p, const Smem<NQ>& sm) {
     }
     __syncthreads();
     if (!*sm.merge_go()) return;
-    const int64_t n_out = p.merge.n_out;
-    const int64_t per = (n_out + gridDim.x - 1) / gridDim.x;
-    const int64_t r0 = static_cast<int64_t>(blockIdx.x) * per;
-    const int64_t r1 = min(n_out, r0 + per);
-    constexpr int kWarps = C::kThreads / 32;
     if (p.merge.merge_stride <= 8) {
-        for (int64_t n = r0 + warp; n < r1; n += kWarps) merge_row<8>(p.merge, n, lane);
+        if (n_first < r1) merge_row_ix<8>(p.merge, n_first, ix0, lane);
+        for (int64_t n = n_first + kWarps; n < r1; n += kWarps) merge_row<8>(p.merge, n, lane);
     } else {
-        for (int64_t n = r0 + warp; n < r1; n += kWarps) merge_row<24>(p.merge, n, lane);
+        if (n_first < r1) merge_row_ix<24>(p.merge, n_first, ix0, lane);
+        for (int64_t n = n_first + kWarps; n < r1; n += kWarps) merge_row<24>(p.merge, n, lane);
     }
 }
 

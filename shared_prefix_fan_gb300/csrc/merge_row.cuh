@@ -21,61 +21,77 @@
 
 namespace fanout {
 
-// One warp merges output row n (a (token, query head) pair). Its partials are
-// either listed in the merge index (planned mode: fixed-stride entry lists
-// {part, row base} per (token, KV head), row = base + g) or uniform
-// (part-major [n_parts][n_out]). The count and the first 32 entries of a row
-// load together; then up to kBatch partials per pass: lane e loads entry e's
-// (m, l) while every lane loads its 4 columns of all the pass's O vectors, so
-// a row of up to kBatch partials costs two memory round trips. Partials are
-// read through L2 (ld.global.cg): in the fused path they were written by other
-// SMs of the same grid.
-template <int kBatch>
-__device__ __forceinline__ void merge_row(const MergeParams& p, int64_t n, int lane) {
-    const bool planned = p.merge_cnt != nullptr;
-    int32_t ne = p.n_parts, g = 0;
-    int64_t key = 0;
-    int2 ent0 = make_int2(0, 0);
-    if (planned) {
+// The merge index of one output row n (a (token, query head) pair): its
+// partial count ne, head-in-group g, and the first 32 entries. Planned mode:
+// fixed-stride entry lists {part, row base} per (token, KV head), partial row
+// = base + g. Uniform mode (merge_cnt null): n_parts partials per row,
+// part-major [n_parts][n_out]. Plan data only, so it may be read before the
+// partials exist.
+struct MergeIdx {
+    int32_t ne, g;
+    int64_t key;
+    int2 ent0;
+};
+__device__ __forceinline__ MergeIdx merge_index(const MergeParams& p, int64_t n, int lane) {
+    MergeIdx ix{p.n_parts, 0, 0, make_int2(0, 0)};
+    if (p.merge_cnt != nullptr) {
         const int H_kv = p.H_q / p.G;
         const int64_t tok = n / p.H_q;
         const int32_t hq = static_cast<int32_t>(n % p.H_q);
-        key = tok * H_kv + hq / p.G;
-        g = hq % p.G;
-        if (lane < p.merge_stride) ent0 = __ldcg(p.merge_ent + key * p.merge_stride + lane);
-        ne = __ldcg(p.merge_cnt + key);
-        if (ne <= 0) return;  // written directly by the attention kernel
+        ix.key = tok * H_kv + hq / p.G;
+        ix.g = hq % p.G;
+        if (lane < p.merge_stride) ix.ent0 = __ldcg(p.merge_ent + ix.key * p.merge_stride + lane);
+        ix.ne = __ldcg(p.merge_cnt + ix.key);
     }
+    return ix;
+}
+
+// One warp merges output row n given its index. Up to kBatch partials per
+// pass: lane e loads entry e's (m, l) while every lane loads its 4 columns of
+// all the pass's O vectors, in one memory round trip. Lanes past the count
+// load a valid duplicate row and get weight 0, so no load result is needed to
+// decide anything before all loads are issued. Partials are read through L2
+// (ld.global.cg): in the fused path they were written by other SMs of the
+// same grid.
+template <int kBatch>
+__device__ __forceinline__ void merge_row_ix(const MergeParams& p, int64_t n,
+                                             const MergeIdx& ix, int lane) {
+    const bool planned = p.merge_cnt != nullptr;
+    const int32_t ne = ix.ne;
+    if (ne <= 0) return;  // written directly by the attention kernel
     float M = -INFINITY, L = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int32_t c0 = 0; c0 < ne; c0 += kBatch) {
         const int32_t cnt = min(kBatch, ne - c0);
-        int64_t my_row = 0;
-        if (lane < cnt) {
-            if (planned) {
-                const int2 en =
-                    (c0 == 0) ? ent0 : __ldcg(p.merge_ent + key * p.merge_stride + c0 + lane);
-                my_row = static_cast<int64_t>(en.x) * p.rows_per_part + en.y + g;
+        const int e = min(lane, cnt - 1);  // lanes past the count repeat the last entry
+        int64_t my_row;
+        if (planned) {
+            int2 en;
+            if (c0 == 0) {  // the first entries are in the index already
+                en.x = __shfl_sync(0xffffffffu, ix.ent0.x, e);
+                en.y = __shfl_sync(0xffffffffu, ix.ent0.y, e);
             } else {
-                my_row = static_cast<int64_t>(c0 + lane) * p.n_out + n;
+                en = __ldcg(p.merge_ent + ix.key * p.merge_stride + c0 + e);
             }
+            my_row = static_cast<int64_t>(en.x) * p.rows_per_part + en.y + ix.g;
+        } else {
+            my_row = static_cast<int64_t>(c0 + e) * p.n_out + n;
         }
-        float2 ml = make_float2(-INFINITY, 0.f);
-        if (lane < cnt) ml = __ldcg(p.part_ml + my_row);
+        const float2 ml_raw = __ldcg(p.part_ml + my_row);
         float4 o[kBatch];
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
-            const int64_t r = __shfl_sync(0xffffffffu, my_row, min(u, cnt - 1));
-            o[u] = (u < cnt) ? __ldcg(reinterpret_cast<const float4*>(p.part_o + r * kHD) + lane)
-                             : make_float4(0.f, 0.f, 0.f, 0.f);
+            const int64_t r = __shfl_sync(0xffffffffu, my_row, u < cnt ? u : cnt - 1);
+            o[u] = __ldcg(reinterpret_cast<const float4*>(p.part_o + r * kHD) + lane);
         }
+        const float2 ml = (lane < cnt) ? ml_raw : make_float2(-INFINITY, 0.f);
         // running (max, sum) over passes, in the base-2 domain
         float mb = (ml.y > 0.f) ? ml.x : -INFINITY;
 #pragma unroll
         for (int s = 16; s > 0; s >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, s));
         const float m_new = fmaxf(M, mb);
         const float corr = (M == -INFINITY) ? 0.f : ptx::ex2(M - m_new);
-        const float w = (ml.y > 0.f) ? ptx::ex2(ml.x - m_new) : 0.f;  // empty shard: 0
+        const float w = (ml.y > 0.f) ? ptx::ex2(ml.x - m_new) : 0.f;  // empty shard / padding: 0
         float lb = w * ml.y;
 #pragma unroll
         for (int s = 16; s > 0; s >>= 1) lb += __shfl_xor_sync(0xffffffffu, lb, s);
@@ -104,6 +120,11 @@ __device__ __forceinline__ void merge_row(const MergeParams& p, int64_t n, int l
             make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
     }
     if (p.lse && lane == 0) p.lse[n] = (M + __log2f(L)) * 0.69314718055994531f;
+}
+
+template <int kBatch>
+__device__ __forceinline__ void merge_row(const MergeParams& p, int64_t n, int lane) {
+    merge_row_ix<kBatch>(p, n, merge_index(p, n, lane), lane);
 }
 
 }  // namespace fanout
