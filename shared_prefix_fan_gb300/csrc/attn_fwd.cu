@@ -582,12 +582,81 @@ __device__ void softmax_group(const SplitParams& p, const Smem<NQ>& sm, uint32_t
 // The log-sum-exp merge of the split-KV partials inside this grid (launched
 // cooperatively, so every CTA is resident): each CTA publishes the call's
 // epoch once its partials are written, waits (bounded) until every CTA has,
-// then merges its slice of the output rows, one warp per row. This replaces
-// the separate merge launch; the per-row arithmetic is merge_row's.
+// then merges a contiguous slice of the output rows. This replaces the
+// separate merge launch.
+//
+// The merge is latency bound (a row needs its index, then its partials), so
+// each warp works on a chunk of rows at a time: it reads the chunk's merge
+// index (plan data: the first chunk's before the wait), then pulls every
+// partial O row of the chunk into its share of the now idle Q + K/V ring with
+// cp.async (16 B per lane, nothing held in registers) and the (m, l) pairs
+// beside them, waits once, and folds each row from shared memory -- in the
+// same passes and order as merge_row, so both paths give the same results. A
+// row with more partials than a warp's share holds falls back to merge_row.
+constexpr int kChunkRows = 8;  // rows whose index a warp reads at once
+
+template <int NQ>
+struct MergeStage {
+    using C = Cfg<NQ>;
+    static constexpr int kWarps = C::kThreads / 32;
+    static constexpr uint32_t kRegion = (C::kSmemBar / kWarps) & ~1023u;  // bytes per warp
+    static constexpr int kSlots = kRegion / (512 + 16);  // partial rows: O + row index + (m, l)
+    static_assert(kSlots <= 96, "(m, l) staging covers three slots per lane");
+    static_assert(kWarps * kRegion <= C::kSmemBar, "staging stays below the barriers");
+};
+
+// A warp's chunk: up to kChunkRows rows from `n`, step kWarps, whose partials
+// fit in the warp's slots. Writes the partial row numbers of the chunk to
+// sidx and returns the rows taken; per row, ne (0: written directly, -1: too
+// many partials, merged by merge_row) and the first slot.
+template <int NQ>
+__device__ __forceinline__ int merge_chunk_index(const SplitParams& p, int64_t n, int64_t r1,
+                                                 int64_t* sidx, int (&ne)[kChunkRows],
+                                                 int (&first)[kChunkRows], int lane) {
+    using M = MergeStage<NQ>;
+    const MergeParams& mp = p.merge;
+    MergeIdx ix[kChunkRows];
+#pragma unroll
+    for (int k = 0; k < kChunkRows; ++k) {  // all index loads of the chunk in flight together
+        const int64_t nk = n + static_cast<int64_t>(k) * M::kWarps;
+        ix[k] = (nk < r1) ? merge_index(mp, nk, lane) : MergeIdx{0, 0, 0, make_int2(0, 0)};
+    }
+    int nslot = 0, rows = 0;
+#pragma unroll
+    for (int k = 0; k < kChunkRows; ++k) {
+        const int64_t nk = n + static_cast<int64_t>(k) * M::kWarps;
+        if (nk >= r1) break;
+        const int c = ix[k].ne;
+        if (c <= 0) {
+            ne[k] = 0;
+        } else if (c > M::kSlots) {
+            ne[k] = -1;
+        } else {
+            if (nslot + c > M::kSlots) break;  // next chunk
+            for (int e = lane; e < c; e += 32) {
+                int64_t pr;
+                if (mp.merge_cnt != nullptr) {
+                    const int2 en = (e < 32) ? ix[k].ent0
+                                             : __ldcg(mp.merge_ent + ix[k].key * mp.merge_stride + e);
+                    pr = static_cast<int64_t>(en.x) * mp.rows_per_part + en.y + ix[k].g;
+                } else {
+                    pr = static_cast<int64_t>(e) * mp.n_out + nk;
+                }
+                sidx[nslot + e] = pr;
+            }
+            ne[k] = c;
+            first[k] = nslot;
+            nslot += c;
+        }
+        rows = k + 1;
+    }
+    return rows;
+}
+
 template <int NQ>
 __device__ void merge_tail(const SplitParams& p, const Smem<NQ>& sm) {
-    using C = Cfg<NQ>;
-    constexpr int kWarps = C::kThreads / 32;
+    using M = MergeStage<NQ>;
+    const MergeParams& mp = p.merge;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     // The __syncthreads before this call orders every partial store of the CTA
@@ -596,15 +665,21 @@ __device__ void merge_tail(const SplitParams& p, const Smem<NQ>& sm) {
         __threadfence();
         ptx::st_release_gpu(p.flags + blockIdx.x, p.epoch);
     }
-    // This CTA's rows; the merge index of each warp's first row is plan data,
-    // read while the other CTAs finish.
-    const int64_t n_out = p.merge.n_out;
+    const int64_t n_out = mp.n_out;
     const int64_t per = (n_out + gridDim.x - 1) / gridDim.x;
     const int64_t r0 = static_cast<int64_t>(blockIdx.x) * per;
     const int64_t r1 = min(n_out, r0 + per);
-    const int64_t n_first = r0 + warp;
-    MergeIdx ix0{0, 0, 0, make_int2(0, 0)};
-    if (n_first < r1) ix0 = merge_index(p.merge, n_first, lane);
+    uint8_t* region = sm.ptr + warp * M::kRegion;
+    const uint32_t region_s = sm.base + warp * M::kRegion;
+    int64_t* sidx = reinterpret_cast<int64_t*>(region + M::kSlots * 512);
+    float2* sml = reinterpret_cast<float2*>(region + M::kSlots * 520);
+    // Every role is done and every MMA / TMA of this CTA has completed: the
+    // ring is free. Order its last async-proxy use before the writes below.
+    ptx::fence_proxy_async_smem();
+    int64_t n = r0 + warp;
+    int ne[kChunkRows], first[kChunkRows];
+    int rows = (n < r1) ? merge_chunk_index<NQ>(p, n, r1, sidx, ne, first, lane) : 0;
+
     if (warp == 0) {
         bool all = false;
         const uint64_t t0 = ptx::globaltimer_ns();
@@ -631,12 +706,79 @@ __device__ void merge_tail(const SplitParams& p, const Smem<NQ>& sm) {
     }
     __syncthreads();
     if (!*sm.merge_go()) return;
-    if (p.merge.merge_stride <= 8) {
-        if (n_first < r1) merge_row_ix<8>(p.merge, n_first, ix0, lane);
-        for (int64_t n = n_first + kWarps; n < r1; n += kWarps) merge_row<8>(p.merge, n, lane);
-    } else {
-        if (n_first < r1) merge_row_ix<24>(p.merge, n_first, ix0, lane);
-        for (int64_t n = n_first + kWarps; n < r1; n += kWarps) merge_row<24>(p.merge, n, lane);
+    __threadfence();  // this thread's reads below come after the grid's partial writes
+    const int kb = (mp.merge_stride <= 8) ? 8 : 24;  // the pass size merge_row uses
+    while (rows > 0) {
+        __syncwarp();  // sidx written by every lane
+        int nslot = 0;
+#pragma unroll
+        for (int k = 0; k < kChunkRows; ++k)
+            if (k < rows && ne[k] > 0) nslot = first[k] + ne[k];
+        float2 mlr[3];  // (m, l) of slots lane, lane + 32, lane + 64, through L2
+#pragma unroll
+        for (int i = 0; i < 3; ++i)
+            if (lane + 32 * i < nslot) mlr[i] = __ldcg(mp.part_ml + sidx[lane + 32 * i]);
+        for (int s2 = 0; s2 < nslot; ++s2)
+            ptx::cp_async_16(region_s + s2 * 512 + lane * 16, mp.part_o + sidx[s2] * kHD + lane * 4);
+#pragma unroll
+        for (int i = 0; i < 3; ++i)
+            if (lane + 32 * i < nslot) sml[lane + 32 * i] = mlr[i];
+        ptx::cp_async_wait_all();
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < kChunkRows; ++k) {
+            if (k >= rows) break;
+            const int64_t nk = n + static_cast<int64_t>(k) * M::kWarps;
+            const int c = ne[k];
+            if (c == 0) continue;
+            if (c < 0) {
+                merge_row<24>(mp, nk, lane);
+                continue;
+            }
+            const float* so = reinterpret_cast<const float*>(region) + first[k] * kHD;
+            float Mx = -INFINITY, L = 0.f;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int c0 = 0; c0 < c; c0 += kb) {
+                const int cnt = min(kb, c - c0);
+                const float2 ml = (lane < cnt) ? sml[first[k] + c0 + lane] : make_float2(-INFINITY, 0.f);
+                float mb = (ml.y > 0.f) ? ml.x : -INFINITY;
+#pragma unroll
+                for (int s = 16; s > 0; s >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, s));
+                const float m_new = fmaxf(Mx, mb);
+                const float corr = (Mx == -INFINITY) ? 0.f : ptx::ex2(Mx - m_new);
+                const float w = (ml.y > 0.f) ? ptx::ex2(ml.x - m_new) : 0.f;
+                float lb = w * ml.y;
+#pragma unroll
+                for (int s = 16; s > 0; s >>= 1) lb += __shfl_xor_sync(0xffffffffu, lb, s);
+                L = L * corr + lb;
+                acc.x *= corr;
+                acc.y *= corr;
+                acc.z *= corr;
+                acc.w *= corr;
+                for (int u = 0; u < cnt; ++u) {
+                    const float wu = __shfl_sync(0xffffffffu, w, u);
+                    const float4 o = reinterpret_cast<const float4*>(so + (c0 + u) * kHD)[lane];
+                    acc.x += wu * o.x;
+                    acc.y += wu * o.y;
+                    acc.z += wu * o.z;
+                    acc.w += wu * o.w;
+                }
+                Mx = m_new;
+            }
+            const float inv = 1.f / L;
+            if (mp.out_bf16) {
+                uint2 v = make_uint2(ptx::pack_bf16x2(acc.x * inv, acc.y * inv),
+                                     ptx::pack_bf16x2(acc.z * inv, acc.w * inv));
+                reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(mp.out) + nk * kHD)[lane] = v;
+            } else {
+                reinterpret_cast<float4*>(static_cast<float*>(mp.out) + nk * kHD)[lane] =
+                    make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+            }
+            if (mp.lse && lane == 0) mp.lse[nk] = (Mx + __log2f(L)) * 0.69314718055994531f;
+        }
+        __syncwarp();  // the slots are read before the next chunk overwrites them
+        n += static_cast<int64_t>(rows) * M::kWarps;
+        rows = (n < r1) ? merge_chunk_index<NQ>(p, n, r1, sidx, ne, first, lane) : 0;
     }
 }
 

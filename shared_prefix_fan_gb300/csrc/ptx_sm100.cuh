@@ -83,6 +83,16 @@ __device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t* p) {
     return v;
 }
 
+// ------------------------------------------------- cp.async (global -> shared)
+// Per-thread asynchronous copies into shared memory (no registers held while
+// in flight); cp_async_wait_all waits for this thread's copies.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ fences
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
