@@ -585,76 +585,79 @@ __device__ void softmax_group(const SplitParams& p, const Smem<NQ>& sm, uint32_t
 // then merges a contiguous slice of the output rows. This replaces the
 // separate merge launch.
 //
-// The merge is latency bound (a row needs its index, then its partials), so
-// each warp works on a chunk of rows at a time: it reads the chunk's merge
-// index (plan data: the first chunk's before the wait), then pulls every
-// partial O row of the chunk into its share of the now idle Q + K/V ring with
-// cp.async (16 B per lane, nothing held in registers) and the (m, l) pairs
-// beside them, waits once, and folds each row from shared memory -- in the
-// same passes and order as merge_row, so both paths give the same results. A
-// row with more partials than a warp's share holds falls back to merge_row.
-constexpr int kChunkRows = 8;  // rows whose index a warp reads at once
+// The merge is latency bound, and this code runs once per launch from a cold
+// instruction cache, so it is written as short rolled loops. Each warp takes
+// its rows in chunks of up to kChunkRows: the chunk's merge index (plan data;
+// the first chunk's read before the wait) costs two round trips, lane k
+// reading row k's count and then every lane one entry; every partial O row of
+// the chunk then comes into the warp's share of the idle Q + K/V ring by
+// cp.async (16 B per lane, nothing held in registers) with the (m, l) pairs
+// beside it, after one wait each row folds from shared memory in the passes
+// and order of merge_row, so both paths give the same results. A row with more
+// partials than the share holds falls back to merge_row.
+constexpr int kChunkRows = 8;
 
 template <int NQ>
 struct MergeStage {
     using C = Cfg<NQ>;
     static constexpr int kWarps = C::kThreads / 32;
     static constexpr uint32_t kRegion = (C::kSmemBar / kWarps) & ~1023u;  // bytes per warp
-    static constexpr int kSlots = kRegion / (512 + 16);  // partial rows: O + row index + (m, l)
-    static_assert(kSlots <= 96, "(m, l) staging covers three slots per lane");
+    static constexpr uint32_t kTab = kChunkRows * 24;  // per row: key (8 B), ne, first, g
+    static constexpr int kSlots = (kRegion - kTab) / (512 + 16);  // O + row index + (m, l)
     static_assert(kWarps * kRegion <= C::kSmemBar, "staging stays below the barriers");
 };
 
-// A warp's chunk: up to kChunkRows rows from `n`, step kWarps, whose partials
-// fit in the warp's slots. Writes the partial row numbers of the chunk to
-// sidx and returns the rows taken; per row, ne (0: written directly, -1: too
-// many partials, merged by merge_row) and the first slot.
+// Reads the merge index of the chunk starting at row n (rows n, n + kWarps,
+// ...), fills the warp's row table and slot list, returns the rows taken.
 template <int NQ>
-__device__ __forceinline__ int merge_chunk_index(const SplitParams& p, int64_t n, int64_t r1,
-                                                 int64_t* sidx, int (&ne)[kChunkRows],
-                                                 int (&first)[kChunkRows], int lane) {
+__device__ __noinline__ int merge_chunk_index(const MergeParams& mp, int64_t n, int64_t r1,
+                                              uint8_t* region, int lane) {
     using M = MergeStage<NQ>;
-    const MergeParams& mp = p.merge;
-    MergeIdx ix[kChunkRows];
-#pragma unroll
-    for (int k = 0; k < kChunkRows; ++k) {  // all index loads of the chunk in flight together
-        const int64_t nk = n + static_cast<int64_t>(k) * M::kWarps;
-        ix[k] = (nk < r1) ? merge_index(mp, nk, lane) : MergeIdx{0, 0, 0, make_int2(0, 0)};
+    int64_t* tkey = reinterpret_cast<int64_t*>(region + M::kSlots * 528);
+    int* tne = reinterpret_cast<int*>(tkey + kChunkRows);
+    int* tfirst = tne + kChunkRows;
+    int* tg = tfirst + kChunkRows;
+    int64_t* sidx = reinterpret_cast<int64_t*>(region + M::kSlots * 512);
+    const int64_t nk = n + static_cast<int64_t>(lane) * M::kWarps;
+    const bool valid = lane < kChunkRows && nk < r1;
+    const int H_kv = mp.H_q / mp.G;
+    int cnt = 0, g = 0;
+    int64_t key = 0;
+    if (valid) {
+        const int64_t tok = nk / mp.H_q;
+        const int hq = static_cast<int>(nk % mp.H_q);
+        key = tok * H_kv + hq / mp.G;
+        g = hq % mp.G;
+        cnt = __ldcg(mp.merge_cnt + key);
     }
-    int nslot = 0, rows = 0;
-#pragma unroll
-    for (int k = 0; k < kChunkRows; ++k) {
-        const int64_t nk = n + static_cast<int64_t>(k) * M::kWarps;
-        if (nk >= r1) break;
-        const int c = ix[k].ne;
-        if (c <= 0) {
-            ne[k] = 0;
-        } else if (c > M::kSlots) {
-            ne[k] = -1;
-        } else {
-            if (nslot + c > M::kSlots) break;  // next chunk
-            for (int e = lane; e < c; e += 32) {
-                int64_t pr;
-                if (mp.merge_cnt != nullptr) {
-                    const int2 en = (e < 32) ? ix[k].ent0
-                                             : __ldcg(mp.merge_ent + ix[k].key * mp.merge_stride + e);
-                    pr = static_cast<int64_t>(en.x) * mp.rows_per_part + en.y + ix[k].g;
-                } else {
-                    pr = static_cast<int64_t>(e) * mp.n_out + nk;
-                }
-                sidx[nslot + e] = pr;
-            }
-            ne[k] = c;
-            first[k] = nslot;
-            nslot += c;
-        }
-        rows = k + 1;
+    const int take = (cnt > 0 && cnt <= M::kSlots) ? cnt : 0;
+    int incl = take;
+    for (int d = 1; d < kChunkRows; d <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += t;
     }
+    const unsigned fit = __ballot_sync(0xffffffffu, valid && incl <= M::kSlots);
+    const int rows = __popc(fit);  // valid rows and fitting rows are both prefixes
+    const int nslot = rows > 0 ? __shfl_sync(0xffffffffu, incl, rows - 1) : 0;
+    if (lane < rows) {
+        tkey[lane] = key;
+        tne[lane] = (cnt > M::kSlots) ? -1 : max(cnt, 0);
+        tfirst[lane] = incl - take;
+        tg[lane] = g;
+    }
+    __syncwarp();
+    for (int s = lane; s < nslot; s += 32) {
+        int k = 0;
+        while (k + 1 < rows && tfirst[k + 1] <= s) ++k;
+        const int2 en = __ldcg(mp.merge_ent + tkey[k] * mp.merge_stride + (s - tfirst[k]));
+        sidx[s] = static_cast<int64_t>(en.x) * mp.rows_per_part + en.y + tg[k];
+    }
+    __syncwarp();
     return rows;
 }
 
 template <int NQ>
-__device__ void merge_tail(const SplitParams& p, const Smem<NQ>& sm) {
+__device__ __noinline__ void merge_tail(const SplitParams& p, const Smem<NQ>& sm) {
     using M = MergeStage<NQ>;
     const MergeParams& mp = p.merge;
     const int warp = threadIdx.x >> 5;
@@ -671,14 +674,16 @@ __device__ void merge_tail(const SplitParams& p, const Smem<NQ>& sm) {
     const int64_t r1 = min(n_out, r0 + per);
     uint8_t* region = sm.ptr + warp * M::kRegion;
     const uint32_t region_s = sm.base + warp * M::kRegion;
+    const float* so = reinterpret_cast<const float*>(region);
     int64_t* sidx = reinterpret_cast<int64_t*>(region + M::kSlots * 512);
     float2* sml = reinterpret_cast<float2*>(region + M::kSlots * 520);
+    const int* tne = reinterpret_cast<const int*>(region + M::kSlots * 528 + kChunkRows * 8);
+    const int* tfirst = tne + kChunkRows;
     // Every role is done and every MMA / TMA of this CTA has completed: the
     // ring is free. Order its last async-proxy use before the writes below.
     ptx::fence_proxy_async_smem();
     int64_t n = r0 + warp;
-    int ne[kChunkRows], first[kChunkRows];
-    int rows = (n < r1) ? merge_chunk_index<NQ>(p, n, r1, sidx, ne, first, lane) : 0;
+    int rows = (n < r1) ? merge_chunk_index<NQ>(mp, n, r1, region, lane) : 0;
 
     if (warp == 0) {
         bool all = false;
@@ -709,46 +714,37 @@ __device__ void merge_tail(const SplitParams& p, const Smem<NQ>& sm) {
     __threadfence();  // this thread's reads below come after the grid's partial writes
     const int kb = (mp.merge_stride <= 8) ? 8 : 24;  // the pass size merge_row uses
     while (rows > 0) {
-        __syncwarp();  // sidx written by every lane
         int nslot = 0;
-#pragma unroll
-        for (int k = 0; k < kChunkRows; ++k)
-            if (k < rows && ne[k] > 0) nslot = first[k] + ne[k];
-        float2 mlr[3];  // (m, l) of slots lane, lane + 32, lane + 64, through L2
-#pragma unroll
-        for (int i = 0; i < 3; ++i)
-            if (lane + 32 * i < nslot) mlr[i] = __ldcg(mp.part_ml + sidx[lane + 32 * i]);
+        for (int k = 0; k < rows; ++k)
+            if (tne[k] > 0) nslot = tfirst[k] + tne[k];
+        for (int s2 = lane; s2 < nslot; s2 += 32) {  // (m, l) through L2 into shared
+            const float2 v = __ldcg(mp.part_ml + sidx[s2]);
+            sml[s2] = v;
+        }
         for (int s2 = 0; s2 < nslot; ++s2)
             ptx::cp_async_16(region_s + s2 * 512 + lane * 16, mp.part_o + sidx[s2] * kHD + lane * 4);
-#pragma unroll
-        for (int i = 0; i < 3; ++i)
-            if (lane + 32 * i < nslot) sml[lane + 32 * i] = mlr[i];
         ptx::cp_async_wait_all();
         __syncwarp();
-#pragma unroll
-        for (int k = 0; k < kChunkRows; ++k) {
-            if (k >= rows) break;
+        for (int k = 0; k < rows; ++k) {
             const int64_t nk = n + static_cast<int64_t>(k) * M::kWarps;
-            const int c = ne[k];
+            const int c = tne[k];
             if (c == 0) continue;
             if (c < 0) {
                 merge_row<24>(mp, nk, lane);
                 continue;
             }
-            const float* so = reinterpret_cast<const float*>(region) + first[k] * kHD;
+            const int f = tfirst[k];
             float Mx = -INFINITY, L = 0.f;
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
             for (int c0 = 0; c0 < c; c0 += kb) {
                 const int cnt = min(kb, c - c0);
-                const float2 ml = (lane < cnt) ? sml[first[k] + c0 + lane] : make_float2(-INFINITY, 0.f);
+                const float2 ml = (lane < cnt) ? sml[f + c0 + lane] : make_float2(-INFINITY, 0.f);
                 float mb = (ml.y > 0.f) ? ml.x : -INFINITY;
-#pragma unroll
                 for (int s = 16; s > 0; s >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, s));
                 const float m_new = fmaxf(Mx, mb);
                 const float corr = (Mx == -INFINITY) ? 0.f : ptx::ex2(Mx - m_new);
                 const float w = (ml.y > 0.f) ? ptx::ex2(ml.x - m_new) : 0.f;
                 float lb = w * ml.y;
-#pragma unroll
                 for (int s = 16; s > 0; s >>= 1) lb += __shfl_xor_sync(0xffffffffu, lb, s);
                 L = L * corr + lb;
                 acc.x *= corr;
@@ -757,7 +753,7 @@ __device__ void merge_tail(const SplitParams& p, const Smem<NQ>& sm) {
                 acc.w *= corr;
                 for (int u = 0; u < cnt; ++u) {
                     const float wu = __shfl_sync(0xffffffffu, w, u);
-                    const float4 o = reinterpret_cast<const float4*>(so + (c0 + u) * kHD)[lane];
+                    const float4 o = reinterpret_cast<const float4*>(so + (f + c0 + u) * kHD)[lane];
                     acc.x += wu * o.x;
                     acc.y += wu * o.y;
                     acc.z += wu * o.z;
@@ -778,7 +774,7 @@ __device__ void merge_tail(const SplitParams& p, const Smem<NQ>& sm) {
         }
         __syncwarp();  // the slots are read before the next chunk overwrites them
         n += static_cast<int64_t>(rows) * M::kWarps;
-        rows = (n < r1) ? merge_chunk_index<NQ>(p, n, r1, sidx, ne, first, lane) : 0;
+        rows = (n < r1) ? merge_chunk_index<NQ>(mp, n, r1, region, lane) : 0;
     }
 }
 
