@@ -63,6 +63,13 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
     }
 }
 
+// Three-input maximum (one instruction on sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 // ------------------------------------------------- grid-scope flag hand-off
 // Release store / acquire load of a 32-bit flag in global memory at GPU scope:
 // writes before the release are visible to a thread whose acquire load reads
