@@ -66,20 +66,26 @@ struct Cfg {
     static constexpr int kTileBytes = kBN * kHD * 2;  // one K or V tile, bf16
     static constexpr int kKVHalf = kTileBytes / 2;    // kBN rows x 64 columns (128 B rows)
     static constexpr int kStages = NQ == 1 ? 6 : 10;
-    static constexpr int kThreads = 64 + 128 * NQ;
+    // Warps: 0 TMA producer, 1 .. NQ one tcgen05 issuer per query tile, then
+    // four softmax warps per query tile (any four consecutive warps cover the
+    // four TMEM lane quarters).
+    static constexpr int kSoftmaxWarp0 = 1 + NQ;
+    static constexpr int kThreads = 32 * kSoftmaxWarp0 + 128 * NQ;
     static constexpr int kSmemQ = 0;
     static constexpr int kSmemRing = kSmemQ + NQ * kQBytes;
     static constexpr int kSmemBar = kSmemRing + kStages * kTileBytes;
     static_assert(kStages <= 32, "stage masks are 32-bit");
     static_assert(kBN == kv_tile_keys(NQ), "host and kernel agree on the tile");
-    // barriers: ring full/empty, Q full/free, aux, drain, then 4 per softmax group
+    // barriers: ring full/empty (a stage is free once every issuer's MMAs that
+    // read it completed: NQ arrivals), Q full/free (NQ arrivals), aux, one
+    // drain per issuer, then 5 per query tile
     static constexpr int BAR_FULL = 0;
     static constexpr int BAR_EMPTY = kStages;
     static constexpr int BAR_QFULL = 2 * kStages;
     static constexpr int BAR_QFREE = BAR_QFULL + 1;
     static constexpr int BAR_AUX = BAR_QFULL + 2;
-    static constexpr int BAR_DRAIN = BAR_QFULL + 3;
-    static constexpr int BAR_GROUP = BAR_QFULL + 4;  // + 5 x + {SFULL, PFULL, ODONE, OFREE, SFREE}
+    static constexpr int BAR_DRAIN = BAR_QFULL + 3;       // + x: issuer x's drain
+    static constexpr int BAR_GROUP = BAR_DRAIN + NQ;  // + 5 x + {SFULL, PFULL, ODONE, OFREE, SFREE}
     static constexpr int kNumBars = BAR_GROUP + 5 * NQ;
     static constexpr int kSmemMisc = kSmemBar + kNumBars * 8;
     static constexpr int kSmemTotal = kSmemMisc + 16;
@@ -275,21 +281,22 @@ __device__ __forceinline__ uint64_t vmn_desc(uint32_t tile_base, uint32_t half_b
     return ptx::sdesc_sw128(tile_base + kk * 2048, half_bytes, 1024);
 }
 
-template <int NQ>
+// Issuer x's position: ring position of the unit's K_0 (K_j at it0 + 2j, V_j at
+// it0 + 2j + 1), tiles and units its query tile processed before this unit.
 struct MmaState {
-    uint32_t it0 = 0;      // ring position of the unit's K_0 (K_j at it0+2j, V_j at it0+2j+1)
-    uint32_t jt[NQ] = {};  // tiles each softmax group processed before this unit
-    int kx[NQ] = {};       // units each softmax group processed before this unit
+    uint32_t it0 = 0;
+    uint32_t jt = 0;
+    int kx = 0;
 };
 
 template <int NQ>
 __device__ __forceinline__ bool issue_s(const SplitParams& p, const Smem<NQ>& sm, uint32_t tmem,
-                                        const MmaState<NQ>& st, int x, int j, uint32_t kb) {
+                                        const MmaState& st, int x, int j, uint32_t kb) {
     using C = Cfg<NQ>;
     // (the TMEM this S overwrites held a P whose P.V was issued earlier)
     ptx::tc_fence_after();
     const uint32_t qb = sm.base + C::kSmemQ + x * kQBytes;
-    const uint32_t d = tmem + s_col<NQ>(x, st.jt[x] + j);
+    const uint32_t d = tmem + s_col<NQ>(x, st.jt + j);
 #pragma unroll
     for (int kk = 0; kk < kHD / 16; ++kk)
         ptx::mma_bf16_ss(d, kmajor_desc(qb, kQHalf, kk), kmajor_desc(kb, C::kKVHalf, kk),
@@ -300,17 +307,17 @@ __device__ __forceinline__ bool issue_s(const SplitParams& p, const Smem<NQ>& sm
 
 template <int NQ>
 __device__ __forceinline__ bool issue_pv(const SplitParams& p, const Smem<NQ>& sm, uint32_t tmem,
-                                         const MmaState<NQ>& st, int x, int jj, uint32_t vb) {
+                                         const MmaState& st, int x, int jj, uint32_t vb) {
     using C = Cfg<NQ>;
     const uint64_t lim = p.wait_limit_ns;
     volatile int* abort = sm.abort_flag();
     // P of tile jj written (and O rescaled) by softmax x; for the unit's first
     // product, the previous unit's O of group x read out.
-    if (!ptx::mbar_wait(sm.gbar(x, PFULL), (st.jt[x] + jj) & 1u, lim, abort)) { record_timeout(p, abort, 14); return false; }
-    if (jj == 0 && st.kx[x] > 0 &&
-        !ptx::mbar_wait(sm.gbar(x, OFREE), (st.kx[x] - 1) & 1, lim, abort)) { record_timeout(p, abort, 15); return false; }
+    if (!ptx::mbar_wait(sm.gbar(x, PFULL), (st.jt + jj) & 1u, lim, abort)) { record_timeout(p, abort, 14); return false; }
+    if (jj == 0 && st.kx > 0 &&
+        !ptx::mbar_wait(sm.gbar(x, OFREE), (st.kx - 1) & 1, lim, abort)) { record_timeout(p, abort, 15); return false; }
     ptx::tc_fence_after();
-    const uint32_t a = tmem + s_col<NQ>(x, st.jt[x] + jj);  // P: kBN / 2 columns of bf16 pairs
+    const uint32_t a = tmem + s_col<NQ>(x, st.jt + jj);  // P: kBN / 2 columns of bf16 pairs
     const uint32_t d = tmem + C::kColO + 128u * x;
 #pragma unroll
     for (int kk = 0; kk < C::kBN / 16; ++kk)
@@ -320,12 +327,21 @@ __device__ __forceinline__ bool issue_pv(const SplitParams& p, const Smem<NQ>& s
     return true;
 }
 
+// Issuer of query tile x (one thread): per K/V tile j, S_x(j) into the S
+// buffer softmax x is not working on (S_x(t) waits until softmax x has read
+// S_x(t-1), so S-full never runs two phases ahead), then P_x.V(j-1) once
+// softmax x has written P_x(j-1). S of a tile thus computes while the softmax
+// of the previous one runs, and each query tile's chain of products waits
+// only on its own softmax. Every issuer takes part in every unit's ring and Q
+// hand-off (a stage or the Q buffers are released by one arrival per issuer),
+// so no issuer can run ahead of the producer; in a unit whose query tile x is
+// empty, issuer x only waits for each stage and releases it.
 template <int NQ>
-__device__ void mma_thread(const SplitParams& p, const Smem<NQ>& sm, uint32_t tmem) {
+__device__ void mma_thread(const SplitParams& p, const Smem<NQ>& sm, uint32_t tmem, int x) {
     using C = Cfg<NQ>;
     const uint64_t lim = p.wait_limit_ns;
     volatile int* abort = sm.abort_flag();
-    MmaState<NQ> st;
+    MmaState st;
     bool ok = true;
     bool issued_any = false;
     int k = 0;
@@ -343,54 +359,49 @@ __device__ void mma_thread(const SplitParams& p, const Smem<NQ>& sm, uint32_t tm
         if (n <= 0) continue;
         const int nq = unit_nq<NQ>(u, p.tpt);
         if (!ptx::mbar_wait(sm.bar(C::BAR_QFULL), k & 1, lim, abort)) { ok = false; record_timeout(p, abort, 10); break; }
-        // Per K/V tile j: S_x(j) for every active query tile x (each into the S
-        // buffer its softmax is not working on: S_x(t) waits until softmax x has
-        // read S_x(t-1), so S-full never runs two phases ahead), then
-        // P_x.V(j-1) for every x once softmax x has written P_x(j-1). The S of a
-        // tile thus computes while the softmax of the previous one runs.
+        if (x >= nq) {  // query tile x is empty in this unit: pass the stages along
+            for (int j = 0; j < n && ok; ++j) {
+                const uint32_t posK = st.it0 + 2u * j;
+                for (uint32_t pos = posK; pos <= posK + 1u && ok; ++pos) {
+                    if (!(ok = wait_full(pos, 16))) break;
+                    ptx::mbar_arrive(sm.bar(C::BAR_EMPTY + stage_of(pos)));
+                }
+            }
+            if (!ok) break;
+            ptx::mbar_arrive(sm.bar(C::BAR_QFREE));
+            st.it0 += 2u * n;
+            ++k;
+            continue;
+        }
         for (int j = 0; j <= n && ok; ++j) {
             const uint32_t posK = st.it0 + 2u * j, posVp = posK - 1u;
             if (j < n) {
                 if (!(ok = wait_full(posK, 11))) break;
-#pragma unroll
-                for (int x = 0; x < NQ; ++x) {
-                    if (x >= nq) break;
-                    const uint32_t t = st.jt[x] + j;
-                    if (t > 0 && !ptx::mbar_wait(sm.gbar(x, SFREE), (t - 1) & 1u, lim, abort)) {
-                        ok = false;
-                        record_timeout(p, abort, 12);
-                        break;
-                    }
-                    issue_s<NQ>(p, sm, tmem, st, x, j, ring(posK));
-                    issued_any = true;
+                const uint32_t t = st.jt + j;
+                if (t > 0 && !ptx::mbar_wait(sm.gbar(x, SFREE), (t - 1) & 1u, lim, abort)) {
+                    ok = false;
+                    record_timeout(p, abort, 12);
+                    break;
                 }
-                if (!ok) break;
+                issue_s<NQ>(p, sm, tmem, st, x, j, ring(posK));
+                issued_any = true;
                 ptx::mma_commit(sm.bar(C::BAR_EMPTY + stage_of(posK)));
                 if (j == n - 1) ptx::mma_commit(sm.bar(C::BAR_QFREE));
             }
             if (j > 0) {
                 if (!(ok = wait_full(posVp, 13))) break;
-#pragma unroll
-                for (int x = 0; x < NQ; ++x) {
-                    if (x >= nq) break;
-                    if (!(ok = issue_pv<NQ>(p, sm, tmem, st, x, j - 1, ring(posVp)))) break;
-                }
-                if (!ok) break;
+                if (!(ok = issue_pv<NQ>(p, sm, tmem, st, x, j - 1, ring(posVp)))) break;
                 ptx::mma_commit(sm.bar(C::BAR_EMPTY + stage_of(posVp)));
             }
         }
         st.it0 += 2u * n;
-        st.jt[0] += n;
-        ++st.kx[0];
-        if (NQ == 2 && nq == 2) {  // static indices keep the counters in registers
-            st.jt[NQ - 1] += n;
-            ++st.kx[NQ - 1];
-        }
+        st.jt += n;
+        ++st.kx;
         ++k;
     }
     if (!ok && issued_any) {
-        ptx::mma_commit(sm.bar(C::BAR_DRAIN));
-        ptx::mbar_wait(sm.bar(C::BAR_DRAIN), 0, lim, nullptr);
+        ptx::mma_commit(sm.bar(C::BAR_DRAIN + x));
+        ptx::mbar_wait(sm.bar(C::BAR_DRAIN + x), 0, lim, nullptr);
     }
 }
 
@@ -799,12 +810,12 @@ __global__ void __launch_bounds__(Cfg<NQ>::kThreads, 1) __maxnreg__(NQ == 2 ? 20
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
             ptx::mbar_init(sm.bar(C::BAR_FULL + s), 1);
-            ptx::mbar_init(sm.bar(C::BAR_EMPTY + s), 1);
+            ptx::mbar_init(sm.bar(C::BAR_EMPTY + s), NQ);  // one commit per issuer
         }
         ptx::mbar_init(sm.bar(C::BAR_QFULL), 1);
-        ptx::mbar_init(sm.bar(C::BAR_QFREE), 1);
+        ptx::mbar_init(sm.bar(C::BAR_QFREE), NQ);
         ptx::mbar_init(sm.bar(C::BAR_AUX), 1);
-        ptx::mbar_init(sm.bar(C::BAR_DRAIN), 1);
+        for (int x = 0; x < NQ; ++x) ptx::mbar_init(sm.bar(C::BAR_DRAIN + x), 1);
         for (int x = 0; x < NQ; ++x) {
             ptx::mbar_init(sm.gbar(x, SFULL), 1);
             ptx::mbar_init(sm.gbar(x, PFULL), 128);
@@ -832,11 +843,11 @@ __global__ void __launch_bounds__(Cfg<NQ>::kThreads, 1) __maxnreg__(NQ == 2 ? 20
 
     if (warp == 0) {
         producer_warp<NQ>(p, sm, &tm_q, &tm_k, &tm_v);
-    } else if (warp == 1) {
-        if (lane == 0) mma_thread<NQ>(p, sm, tmem);
+    } else if (warp < C::kSoftmaxWarp0) {
+        if (lane == 0) mma_thread<NQ>(p, sm, tmem, warp - 1);
         __syncwarp();
     } else {
-        softmax_group<NQ>(p, sm, tmem, (warp - 2) >> 2);
+        softmax_group<NQ>(p, sm, tmem, (warp - C::kSoftmaxWarp0) >> 2);
     }
 
     ptx::tc_fence_before();
