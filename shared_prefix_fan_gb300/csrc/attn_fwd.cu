@@ -59,13 +59,10 @@ constexpr int kErrTimeout = 5;        // FANOUT_ETIMEOUT
 
 template <int NQ>
 struct Cfg {
-    // Keys per K/V tile: 128 for one query tile; 64 for two, so that each
-    // softmax group gets two S buffers in TMEM (S of the next tile computes
-    // while the softmax works on this one; 2 x 2 x 64 S columns + 2 x 128 O).
-    static constexpr int kBN = NQ == 2 ? 64 : 128;
+    static constexpr int kBN = 128;  // keys per K/V tile
     static constexpr int kTileBytes = kBN * kHD * 2;  // one K or V tile, bf16
     static constexpr int kKVHalf = kTileBytes / 2;    // kBN rows x 64 columns (128 B rows)
-    static constexpr int kStages = NQ == 1 ? 6 : 10;
+    static constexpr int kStages = NQ == 1 ? 6 : 5;
     // Warps: 0 TMA producer, 1 .. NQ one tcgen05 issuer per query tile, then
     // four softmax warps per query tile (any four consecutive warps cover the
     // four TMEM lane quarters).
@@ -101,11 +98,12 @@ template <int NQ>
 constexpr uint32_t idesc_qk() { return ptx::idesc_bf16_f32(kBM, Cfg<NQ>::kBN, false, false); }
 constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(kBM, kHD, false, true);
 
-// TMEM column of the S (and P) buffer group x uses for its t-th tile: two
-// buffers per group, alternating by tile parity.
+// TMEM column of the S (and P) buffer group x uses for its t-th tile: one
+// query tile has two S buffers alternating by tile parity; with two query
+// tiles each has one (2 x 128 S columns + 2 x 128 O columns fill TMEM).
 template <int NQ>
 __device__ __forceinline__ uint32_t s_col(int x, uint32_t t) {
-    return NQ == 2 ? 128u * x + 64u * (t & 1u) : 128u * (t & 1u);
+    return NQ == 2 ? 128u * x : 128u * (t & 1u);
 }
 
 template <int NQ>
@@ -327,12 +325,16 @@ __device__ __forceinline__ bool issue_pv(const SplitParams& p, const Smem<NQ>& s
     return true;
 }
 
-// Issuer of query tile x (one thread): per K/V tile j, S_x(j) into the S
-// buffer softmax x is not working on (S_x(t) waits until softmax x has read
-// S_x(t-1), so S-full never runs two phases ahead), then P_x.V(j-1) once
-// softmax x has written P_x(j-1). S of a tile thus computes while the softmax
-// of the previous one runs, and each query tile's chain of products waits
-// only on its own softmax. Every issuer takes part in every unit's ring and Q
+// Issuer of query tile x (one thread). One query tile (two S buffers): per
+// K/V tile j, S(j) into the buffer the softmax is not working on (S(t) waits
+// until the softmax has read S(t-1), so S-full never runs two phases ahead),
+// then P.V(j-1) once the softmax has written P(j-1): S of a tile computes
+// while the softmax of the previous one runs. Two query tiles (one S buffer
+// each, P written over S): S_x(0), then per tile P_x.V(j) once softmax x has
+// written P_x(j), followed by S_x(j+1) into the same buffer; each query
+// tile's chain of products waits only on its own softmax, and while one
+// softmax works the tensor core runs the other tile's products. Every issuer
+// takes part in every unit's ring and Q
 // hand-off (a stage or the Q buffers are released by one arrival per issuer),
 // so no issuer can run ahead of the producer; in a unit whose query tile x is
 // empty, issuer x only waits for each stage and releases it.
@@ -373,25 +375,48 @@ __device__ void mma_thread(const SplitParams& p, const Smem<NQ>& sm, uint32_t tm
             ++k;
             continue;
         }
-        for (int j = 0; j <= n && ok; ++j) {
-            const uint32_t posK = st.it0 + 2u * j, posVp = posK - 1u;
-            if (j < n) {
-                if (!(ok = wait_full(posK, 11))) break;
-                const uint32_t t = st.jt + j;
-                if (t > 0 && !ptx::mbar_wait(sm.gbar(x, SFREE), (t - 1) & 1u, lim, abort)) {
-                    ok = false;
-                    record_timeout(p, abort, 12);
-                    break;
+        if (NQ == 2) {
+            for (int j = 0; j < n && ok; ++j) {
+                const uint32_t posK = st.it0 + 2u * j, posV = posK + 1u;
+                if (j == 0) {  // S_x(0); later S_x(j) follow P_x.V(j-1) below
+                    if (!(ok = wait_full(posK, 11))) break;
+                    issue_s<NQ>(p, sm, tmem, st, x, 0, ring(posK));
+                    issued_any = true;
+                    ptx::mma_commit(sm.bar(C::BAR_EMPTY + stage_of(posK)));
+                    if (n == 1) ptx::mma_commit(sm.bar(C::BAR_QFREE));
                 }
-                issue_s<NQ>(p, sm, tmem, st, x, j, ring(posK));
-                issued_any = true;
-                ptx::mma_commit(sm.bar(C::BAR_EMPTY + stage_of(posK)));
-                if (j == n - 1) ptx::mma_commit(sm.bar(C::BAR_QFREE));
+                if (!(ok = wait_full(posV, 13))) break;
+                if (!(ok = issue_pv<NQ>(p, sm, tmem, st, x, j, ring(posV)))) break;
+                ptx::mma_commit(sm.bar(C::BAR_EMPTY + stage_of(posV)));
+                if (j + 1 < n) {
+                    const uint32_t posK1 = posK + 2u;
+                    if (!(ok = wait_full(posK1, 11))) break;
+                    issue_s<NQ>(p, sm, tmem, st, x, j + 1, ring(posK1));
+                    ptx::mma_commit(sm.bar(C::BAR_EMPTY + stage_of(posK1)));
+                    if (j + 1 == n - 1) ptx::mma_commit(sm.bar(C::BAR_QFREE));
+                }
             }
-            if (j > 0) {
-                if (!(ok = wait_full(posVp, 13))) break;
-                if (!(ok = issue_pv<NQ>(p, sm, tmem, st, x, j - 1, ring(posVp)))) break;
-                ptx::mma_commit(sm.bar(C::BAR_EMPTY + stage_of(posVp)));
+        } else {
+            for (int j = 0; j <= n && ok; ++j) {
+                const uint32_t posK = st.it0 + 2u * j, posVp = posK - 1u;
+                if (j < n) {
+                    if (!(ok = wait_full(posK, 11))) break;
+                    const uint32_t t = st.jt + j;
+                    if (t > 0 && !ptx::mbar_wait(sm.gbar(x, SFREE), (t - 1) & 1u, lim, abort)) {
+                        ok = false;
+                        record_timeout(p, abort, 12);
+                        break;
+                    }
+                    issue_s<NQ>(p, sm, tmem, st, x, j, ring(posK));
+                    issued_any = true;
+                    ptx::mma_commit(sm.bar(C::BAR_EMPTY + stage_of(posK)));
+                    if (j == n - 1) ptx::mma_commit(sm.bar(C::BAR_QFREE));
+                }
+                if (j > 0) {
+                    if (!(ok = wait_full(posVp, 13))) break;
+                    if (!(ok = issue_pv<NQ>(p, sm, tmem, st, x, j - 1, ring(posVp)))) break;
+                    ptx::mma_commit(sm.bar(C::BAR_EMPTY + stage_of(posVp)));
+                }
             }
         }
         st.it0 += 2u * n;
@@ -448,9 +473,11 @@ __device__ void softmax_group(const SplitParams& p, const Smem<NQ>& sm, uint32_t
             bool w = ptx::mbar_wait(sm.gbar(x, SFULL), jt & 1u, lim, abort);
             if (!__all_sync(0xffffffffu, w)) { ok = false; record_timeout(p, abort, 20); break; }
             ptx::tc_fence_after();
-            // S(jt) seen: the MMA may issue S(jt+1) into the other S buffer (its
-            // S-full then cannot run two phases ahead of this wait).
-            ptx::mbar_arrive(sm.gbar(x, SFREE));
+            if (NQ == 1) {
+                // S(jt) seen: the MMA may issue S(jt+1) into the other S buffer
+                // (its S-full then cannot run two phases ahead of this wait).
+                ptx::mbar_arrive(sm.gbar(x, SFREE));
+            }
             const uint32_t colS = s_col<NQ>(x, jt);
             float corr = 1.f;
             if (active) {
@@ -506,15 +533,18 @@ __device__ void softmax_group(const SplitParams& p, const Smem<NQ>& sm, uint32_t
                 l_run = l_run * corr + sum8(sm8);
                 ptx::tmem_st_wait();
             }
-            if (j > 0) {
-                // The previous P.V must be done before O is rescaled in place; waiting
-                // for it every tile also keeps P-full from running two phases ahead
-                // of the MMA thread (it is normally complete already).
+            // The previous P.V must be done before O is rescaled in place. With one
+            // query tile the wait comes every tile: it also keeps P-full from
+            // running two phases ahead of the issuer (S of the next tile does not
+            // wait for P.V). With two, S_x(j+1) follows P_x.V(j), so only a rescale
+            // needs it; the P.V is normally complete already.
+            const bool rescale = j > 0 && __any_sync(0xffffffffu, corr != 1.f);
+            if (j > 0 && (NQ == 1 || rescale)) {
                 w = ptx::mbar_wait(sm.gbar(x, ODONE), (jt - 1) & 1u, lim, abort);
                 if (!__all_sync(0xffffffffu, w)) { ok = false; record_timeout(p, abort, 21); break; }
                 ptx::tc_fence_after();
             }
-            if (j > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
+            if (rescale) {
                 uint32_t r[32];
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
