@@ -52,37 +52,27 @@
 namespace fanout {
 namespace {
 
+constexpr int kTileBytes = kBN * kHD * 2;   // one K or V tile, bf16
+constexpr int kHalfBytes = kTileBytes / 2;  // 128 rows x 64 columns (128 B rows)
 constexpr int kQBytes = kBM * kHD * 2;
-constexpr int kQHalf = kQBytes / 2;  // 128 rows x 64 columns (128 B rows)
 constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold (base-2 units)
 constexpr int kErrTimeout = 5;        // FANOUT_ETIMEOUT
 
 template <int NQ>
 struct Cfg {
-    static constexpr int kBN = 128;  // keys per K/V tile
-    static constexpr int kTileBytes = kBN * kHD * 2;  // one K or V tile, bf16
-    static constexpr int kKVHalf = kTileBytes / 2;    // kBN rows x 64 columns (128 B rows)
     static constexpr int kStages = NQ == 1 ? 6 : 5;
-    // Warps: 0 TMA producer, 1 .. NQ one tcgen05 issuer per query tile, then
-    // four softmax warps per query tile (any four consecutive warps cover the
-    // four TMEM lane quarters).
-    static constexpr int kSoftmaxWarp0 = 1 + NQ;
-    static constexpr int kThreads = 32 * kSoftmaxWarp0 + 128 * NQ;
+    static constexpr int kThreads = 64 + 128 * NQ;
     static constexpr int kSmemQ = 0;
     static constexpr int kSmemRing = kSmemQ + NQ * kQBytes;
     static constexpr int kSmemBar = kSmemRing + kStages * kTileBytes;
-    static_assert(kStages <= 32, "stage masks are 32-bit");
-    static_assert(kBN == kv_tile_keys(NQ), "host and kernel agree on the tile");
-    // barriers: ring full/empty (a stage is free once every issuer's MMAs that
-    // read it completed: NQ arrivals), Q full/free (NQ arrivals), aux, one
-    // drain per issuer, then 5 per query tile
+    // barriers: ring full/empty, Q full/free, aux, drain, then 4 per softmax group
     static constexpr int BAR_FULL = 0;
     static constexpr int BAR_EMPTY = kStages;
     static constexpr int BAR_QFULL = 2 * kStages;
     static constexpr int BAR_QFREE = BAR_QFULL + 1;
     static constexpr int BAR_AUX = BAR_QFULL + 2;
-    static constexpr int BAR_DRAIN = BAR_QFULL + 3;       // + x: issuer x's drain
-    static constexpr int BAR_GROUP = BAR_DRAIN + NQ;  // + 5 x + {SFULL, PFULL, ODONE, OFREE, SFREE}
+    static constexpr int BAR_DRAIN = BAR_QFULL + 3;
+    static constexpr int BAR_GROUP = BAR_QFULL + 4;  // + 5 x + {SFULL, PFULL, ODONE, OFREE, SFREE}
     static constexpr int kNumBars = BAR_GROUP + 5 * NQ;
     static constexpr int kSmemMisc = kSmemBar + kNumBars * 8;
     static constexpr int kSmemTotal = kSmemMisc + 16;
@@ -94,13 +84,10 @@ struct Cfg {
 
 enum { SFULL = 0, PFULL = 1, ODONE = 2, OFREE = 3, SFREE = 4 };
 
-template <int NQ>
-constexpr uint32_t idesc_qk() { return ptx::idesc_bf16_f32(kBM, Cfg<NQ>::kBN, false, false); }
+constexpr uint32_t kIdescQK = ptx::idesc_bf16_f32(kBM, kBN, false, false);
 constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(kBM, kHD, false, true);
 
-// TMEM column of the S (and P) buffer group x uses for its t-th tile: one
-// query tile has two S buffers alternating by tile parity; with two query
-// tiles each has one (2 x 128 S columns + 2 x 128 O columns fill TMEM).
+// TMEM column of the S (and P) buffer group x uses for its t-th tile.
 template <int NQ>
 __device__ __forceinline__ uint32_t s_col(int x, uint32_t t) {
     return NQ == 2 ? 128u * x : 128u * (t & 1u);
@@ -131,9 +118,8 @@ __device__ __forceinline__ void record_timeout(const SplitParams& p, volatile in
     }
 }
 
-template <int NQ>
 __device__ __forceinline__ int unit_tiles(const Unit& u) {
-    return (u.key_end - u.key_begin + Cfg<NQ>::kBN - 1) / Cfg<NQ>::kBN;
+    return (u.key_end - u.key_begin + kBN - 1) / kBN;
 }
 
 // Query tiles of a unit that hold at least one row.
@@ -161,7 +147,7 @@ __device__ void producer_warp(const SplitParams& p, const Smem<NQ>& sm, const CU
     int k = 0;
     for (int ui = p.cta_first[blockIdx.x]; ui < p.cta_first[blockIdx.x + 1] && ok; ++ui) {
         const Unit u = p.units[ui];
-        const int n_tiles = unit_tiles<NQ>(u);
+        const int n_tiles = unit_tiles(u);
         if (n_tiles <= 0) continue;
         const int nq = unit_nq<NQ>(u, p.tpt);
         // Q tiles: the Q buffers are free once the previous unit's last S MMA completed.
@@ -178,7 +164,7 @@ __device__ void producer_warp(const SplitParams& p, const Smem<NQ>& sm, const CU
                 const uint32_t dst = sm.base + C::kSmemQ + x * kQBytes;
                 const int z = u.tok_begin + x * p.tpt;
                 ptx::tma_load_3d(dst, tm_q, qb, 0, y, z);
-                ptx::tma_load_3d(dst + kQHalf, tm_q, qb, 64, y, z);
+                ptx::tma_load_3d(dst + kHalfBytes, tm_q, qb, 64, y, z);
             }
         }
         // Page ids of the unit, 32 per window (lane l holds page l of the window),
@@ -186,9 +172,7 @@ __device__ void producer_warp(const SplitParams& p, const Smem<NQ>& sm, const CU
         const int32_t* prow = p.page_table + static_cast<int64_t>(u.branch) * p.max_pages +
                               u.key_begin / ps;
         const int n_pages_unit = (u.key_end - u.key_begin + ps - 1) / ps;
-        // A tile is kBN keys: kBN / ps whole pages, or (pages larger than a tile)
-        // one box of kBN rows at an offset inside a page.
-        const int box_rows = min(ps, C::kBN);
+        const int ppt = kBN / ps;  // pages per tile: 1, 2, 4 or 8 (divides 32)
         auto load_window = [&](int w) -> int {
             const int idx = w * 32 + lane;
             return idx < n_pages_unit ? __ldg(prow + idx) : 0;
@@ -197,11 +181,10 @@ __device__ void producer_warp(const SplitParams& p, const Smem<NQ>& sm, const CU
         int win_cur = load_window(0);
         int win_nxt = load_window(1);
         for (int j = 0; j < n_tiles && ok; ++j) {
-            const int kt = u.key_begin + j * C::kBN;
-            const int n_valid = min(C::kBN, u.key_end - kt);
-            const int n_pg = (n_valid + box_rows - 1) / box_rows;  // boxes to load
-            const int rel = (j * C::kBN) / ps;   // first page of the tile, relative to the unit
-            const int in_page = (j * C::kBN) % ps;  // first row inside it (pages > tile)
+            const int kt = u.key_begin + j * kBN;
+            const int n_valid = min(kBN, u.key_end - kt);
+            const int n_pg = (n_valid + ps - 1) / ps;
+            const int rel = j * ppt;  // first page of the tile, relative to the unit
             if ((rel >> 5) != win) {
                 win = rel >> 5;
                 win_cur = win_nxt;
@@ -214,19 +197,18 @@ __device__ void producer_warp(const SplitParams& p, const Smem<NQ>& sm, const CU
                 bool w = true;
                 if (lane == 0) w = ptx::mbar_wait(sm.bar(C::BAR_EMPTY + stage), par ^ 1u, lim, abort);
                 if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; if (lane == 0) record_timeout(p, abort, 2); break; }
-                const uint32_t dst = sm.base + C::kSmemRing + stage * C::kTileBytes;
+                const uint32_t dst = sm.base + C::kSmemRing + stage * kTileBytes;
                 const CUtensorMap* tm = kv == 0 ? tm_k : tm_v;
-                const bool partial = n_valid < C::kBN;
+                const bool partial = n_valid < kBN;
                 const uint32_t bar = partial ? sm.bar(C::BAR_AUX) : sm.bar(C::BAR_FULL + stage);
-                if (lane == 0)
-                    ptx::mbar_arrive_expect_tx(bar, static_cast<uint32_t>(n_pg * box_rows) * 256u);
+                if (lane == 0) ptx::mbar_arrive_expect_tx(bar, static_cast<uint32_t>(n_pg * ps) * 256u);
                 for (int pg = 0; pg < n_pg; ++pg) {
                     const int page = __shfl_sync(0xffffffffu, win_cur, pg_off + pg);
                     if (lane == 0) {
-                        const int row = (page * p.H_kv + u.kv_head) * ps + in_page;
-                        const uint32_t off = static_cast<uint32_t>(pg * box_rows) * 128u;
+                        const int row = (page * p.H_kv + u.kv_head) * ps;
+                        const uint32_t off = static_cast<uint32_t>(pg * ps) * 128u;
                         ptx::tma_load_2d(dst + off, tm, bar, 0, row);
-                        ptx::tma_load_2d(dst + C::kKVHalf + off, tm, bar, 64, row);
+                        ptx::tma_load_2d(dst + kHalfBytes + off, tm, bar, 64, row);
                     }
                 }
                 if (lane == 0) {
@@ -242,11 +224,11 @@ __device__ void producer_warp(const SplitParams& p, const Smem<NQ>& sm, const CU
                     if (!__shfl_sync(0xffffffffu, w2, 0)) { ok = false; if (lane == 0) record_timeout(p, abort, 3); break; }
                     aux_pending = false;
                     aux_phase ^= 1u;
-                    const int n_zero = (C::kBN - n_valid) * 16;  // 16-byte chunks, both halves
+                    const int n_zero = (kBN - n_valid) * 16;  // 16-byte chunks, both halves
                     for (int idx = lane; idx < n_zero; idx += 32) {
                         const int r = n_valid + (idx >> 4);
                         const int ch = idx & 15;
-                        const uint32_t a = dst + (ch >> 3) * C::kKVHalf + r * 128 + (ch & 7) * 16;
+                        const uint32_t a = dst + (ch >> 3) * kHalfBytes + r * 128 + (ch & 7) * 16;
                         ptx::st_shared_v4(a, 0u, 0u, 0u, 0u);
                     }
                     ptx::fence_proxy_async_smem();
@@ -267,83 +249,67 @@ __device__ void producer_warp(const SplitParams& p, const Smem<NQ>& sm, const CU
 }
 
 // ------------------------------------------------------------------ MMA issuer
-__device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile_base, uint32_t half_bytes, int kk) {
-    // K-major, 128-byte swizzle: 64-column halves half_bytes apart, 8-row groups
-    // 1 KB apart; a 16-element K step advances 32 bytes inside the swizzle atom.
-    return ptx::sdesc_sw128(tile_base + (kk >> 2) * half_bytes + (kk & 3) * 32, 16, 1024);
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile_base, int kk) {
+    // K-major, 128-byte swizzle: 64-column halves 16 KB apart, 8-row groups 1 KB
+    // apart; a 16-element K step advances 32 bytes inside the swizzle atom.
+    return ptx::sdesc_sw128(tile_base + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
 }
-__device__ __forceinline__ uint64_t vmn_desc(uint32_t tile_base, uint32_t half_bytes, int kk) {
+__device__ __forceinline__ uint64_t vmn_desc(uint32_t tile_base, int kk) {
     // V as the B operand of P.V: MN-major (d contiguous), 128-byte swizzle.
     // LBO = distance between 64-column halves, SBO = between 8-key groups;
     // a 16-key K step advances 16 rows = 2 KB.
-    return ptx::sdesc_sw128(tile_base + kk * 2048, half_bytes, 1024);
+    return ptx::sdesc_sw128(tile_base + kk * 2048, kHalfBytes, 1024);
 }
 
-// Issuer x's position: ring position of the unit's K_0 (K_j at it0 + 2j, V_j at
-// it0 + 2j + 1), tiles and units its query tile processed before this unit.
+template <int NQ>
 struct MmaState {
-    uint32_t it0 = 0;
-    uint32_t jt = 0;
-    int kx = 0;
+    uint32_t it0 = 0;      // ring position of the unit's K_0 (K_j at it0+2j, V_j at it0+2j+1)
+    uint32_t jt[NQ] = {};  // tiles each softmax group processed before this unit
+    int kx[NQ] = {};       // units each softmax group processed before this unit
 };
 
 template <int NQ>
 __device__ __forceinline__ bool issue_s(const SplitParams& p, const Smem<NQ>& sm, uint32_t tmem,
-                                        const MmaState& st, int x, int j, uint32_t kb) {
+                                        const MmaState<NQ>& st, int x, int j, uint32_t kb) {
     using C = Cfg<NQ>;
     // (the TMEM this S overwrites held a P whose P.V was issued earlier)
     ptx::tc_fence_after();
     const uint32_t qb = sm.base + C::kSmemQ + x * kQBytes;
-    const uint32_t d = tmem + s_col<NQ>(x, st.jt + j);
+    const uint32_t d = tmem + s_col<NQ>(x, st.jt[x] + j);
 #pragma unroll
     for (int kk = 0; kk < kHD / 16; ++kk)
-        ptx::mma_bf16_ss(d, kmajor_desc(qb, kQHalf, kk), kmajor_desc(kb, C::kKVHalf, kk),
-                         idesc_qk<NQ>(), kk > 0);
+        ptx::mma_bf16_ss(d, kmajor_desc(qb, kk), kmajor_desc(kb, kk), kIdescQK, kk > 0);
     ptx::mma_commit(sm.gbar(x, SFULL));
     return true;
 }
 
 template <int NQ>
 __device__ __forceinline__ bool issue_pv(const SplitParams& p, const Smem<NQ>& sm, uint32_t tmem,
-                                         const MmaState& st, int x, int jj, uint32_t vb) {
+                                         const MmaState<NQ>& st, int x, int jj, uint32_t vb) {
     using C = Cfg<NQ>;
     const uint64_t lim = p.wait_limit_ns;
     volatile int* abort = sm.abort_flag();
     // P of tile jj written (and O rescaled) by softmax x; for the unit's first
     // product, the previous unit's O of group x read out.
-    if (!ptx::mbar_wait(sm.gbar(x, PFULL), (st.jt + jj) & 1u, lim, abort)) { record_timeout(p, abort, 14); return false; }
-    if (jj == 0 && st.kx > 0 &&
-        !ptx::mbar_wait(sm.gbar(x, OFREE), (st.kx - 1) & 1, lim, abort)) { record_timeout(p, abort, 15); return false; }
+    if (!ptx::mbar_wait(sm.gbar(x, PFULL), (st.jt[x] + jj) & 1u, lim, abort)) { record_timeout(p, abort, 14); return false; }
+    if (jj == 0 && st.kx[x] > 0 &&
+        !ptx::mbar_wait(sm.gbar(x, OFREE), (st.kx[x] - 1) & 1, lim, abort)) { record_timeout(p, abort, 15); return false; }
     ptx::tc_fence_after();
-    const uint32_t a = tmem + s_col<NQ>(x, st.jt + jj);  // P: kBN / 2 columns of bf16 pairs
+    const uint32_t a = tmem + s_col<NQ>(x, st.jt[x] + jj);  // P: 64 columns of bf16 pairs
     const uint32_t d = tmem + C::kColO + 128u * x;
 #pragma unroll
-    for (int kk = 0; kk < C::kBN / 16; ++kk)
-        ptx::mma_bf16_ts(d, a + 8u * kk, vmn_desc(vb, C::kKVHalf, kk), kIdescPV,
-                         (jj > 0 || kk > 0) ? 1u : 0u);
+    for (int kk = 0; kk < kBN / 16; ++kk)
+        ptx::mma_bf16_ts(d, a + 8u * kk, vmn_desc(vb, kk), kIdescPV, (jj > 0 || kk > 0) ? 1u : 0u);
     ptx::mma_commit(sm.gbar(x, ODONE));
     return true;
 }
 
-// Issuer of query tile x (one thread). One query tile (two S buffers): per
-// K/V tile j, S(j) into the buffer the softmax is not working on (S(t) waits
-// until the softmax has read S(t-1), so S-full never runs two phases ahead),
-// then P.V(j-1) once the softmax has written P(j-1): S of a tile computes
-// while the softmax of the previous one runs. Two query tiles (one S buffer
-// each, P written over S): S_x(0), then per tile P_x.V(j) once softmax x has
-// written P_x(j), followed by S_x(j+1) into the same buffer; each query
-// tile's chain of products waits only on its own softmax, and while one
-// softmax works the tensor core runs the other tile's products. Every issuer
-// takes part in every unit's ring and Q
-// hand-off (a stage or the Q buffers are released by one arrival per issuer),
-// so no issuer can run ahead of the producer; in a unit whose query tile x is
-// empty, issuer x only waits for each stage and releases it.
 template <int NQ>
-__device__ void mma_thread(const SplitParams& p, const Smem<NQ>& sm, uint32_t tmem, int x) {
+__device__ void mma_thread(const SplitParams& p, const Smem<NQ>& sm, uint32_t tmem) {
     using C = Cfg<NQ>;
     const uint64_t lim = p.wait_limit_ns;
     volatile int* abort = sm.abort_flag();
-    MmaState st;
+    MmaState<NQ> st;
     bool ok = true;
     bool issued_any = false;
     int k = 0;
@@ -354,79 +320,80 @@ __device__ void mma_thread(const SplitParams& p, const Smem<NQ>& sm, uint32_t tm
         record_timeout(p, abort, site);
         return false;
     };
-    auto ring = [&](uint32_t pos) { return sm.base + C::kSmemRing + stage_of(pos) * C::kTileBytes; };
+    auto ring = [&](uint32_t pos) { return sm.base + C::kSmemRing + stage_of(pos) * kTileBytes; };
     for (int ui = p.cta_first[blockIdx.x]; ui < p.cta_first[blockIdx.x + 1] && ok; ++ui) {
         const Unit u = p.units[ui];
-        const int n = unit_tiles<NQ>(u);
+        const int n = unit_tiles(u);
         if (n <= 0) continue;
         const int nq = unit_nq<NQ>(u, p.tpt);
         if (!ptx::mbar_wait(sm.bar(C::BAR_QFULL), k & 1, lim, abort)) { ok = false; record_timeout(p, abort, 10); break; }
-        if (x >= nq) {  // query tile x is empty in this unit: pass the stages along
-            for (int j = 0; j < n && ok; ++j) {
-                const uint32_t posK = st.it0 + 2u * j;
-                for (uint32_t pos = posK; pos <= posK + 1u && ok; ++pos) {
-                    if (!(ok = wait_full(pos, 16))) break;
-                    ptx::mbar_arrive(sm.bar(C::BAR_EMPTY + stage_of(pos)));
-                }
-            }
-            if (!ok) break;
-            ptx::mbar_arrive(sm.bar(C::BAR_QFREE));
-            st.it0 += 2u * n;
-            ++k;
-            continue;
-        }
-        if (NQ == 2) {
-            for (int j = 0; j < n && ok; ++j) {
-                const uint32_t posK = st.it0 + 2u * j, posV = posK + 1u;
-                if (j == 0) {  // S_x(0); later S_x(j) follow P_x.V(j-1) below
-                    if (!(ok = wait_full(posK, 11))) break;
-                    issue_s<NQ>(p, sm, tmem, st, x, 0, ring(posK));
-                    issued_any = true;
-                    ptx::mma_commit(sm.bar(C::BAR_EMPTY + stage_of(posK)));
-                    if (n == 1) ptx::mma_commit(sm.bar(C::BAR_QFREE));
-                }
-                if (!(ok = wait_full(posV, 13))) break;
-                if (!(ok = issue_pv<NQ>(p, sm, tmem, st, x, j, ring(posV)))) break;
-                ptx::mma_commit(sm.bar(C::BAR_EMPTY + stage_of(posV)));
-                if (j + 1 < n) {
-                    const uint32_t posK1 = posK + 2u;
-                    if (!(ok = wait_full(posK1, 11))) break;
-                    issue_s<NQ>(p, sm, tmem, st, x, j + 1, ring(posK1));
-                    ptx::mma_commit(sm.bar(C::BAR_EMPTY + stage_of(posK1)));
-                    if (j + 1 == n - 1) ptx::mma_commit(sm.bar(C::BAR_QFREE));
-                }
-            }
-        } else {
-            for (int j = 0; j <= n && ok; ++j) {
-                const uint32_t posK = st.it0 + 2u * j, posVp = posK - 1u;
+        for (int j = 0; j <= n && ok; ++j) {
+            const uint32_t posK = st.it0 + 2u * j, posV = posK + 1u, posVp = posK - 1u;
+            if (NQ == 2 && nq == 2) {
+                // S_0(j), P.V_1(j-1), S_1(j), P.V_0(j)
                 if (j < n) {
                     if (!(ok = wait_full(posK, 11))) break;
-                    const uint32_t t = st.jt + j;
-                    if (t > 0 && !ptx::mbar_wait(sm.gbar(x, SFREE), (t - 1) & 1u, lim, abort)) {
+                    issue_s<NQ>(p, sm, tmem, st, 0, j, ring(posK));
+                    issued_any = true;
+                }
+                if (j > 0) {
+                    if (!(ok = issue_pv<NQ>(p, sm, tmem, st, 1, j - 1, ring(posVp)))) break;
+                    ptx::mma_commit(sm.bar(C::BAR_EMPTY + stage_of(posVp)));
+                }
+                if (j < n) {
+                    issue_s<NQ>(p, sm, tmem, st, 1, j, ring(posK));
+                    ptx::mma_commit(sm.bar(C::BAR_EMPTY + stage_of(posK)));
+                    if (j == n - 1) ptx::mma_commit(sm.bar(C::BAR_QFREE));
+                    if (!(ok = wait_full(posV, 13))) break;
+                    if (!(ok = issue_pv<NQ>(p, sm, tmem, st, 0, j, ring(posV)))) break;
+                }
+            } else if (NQ == 2) {
+                // one query tile only: S_0(j), P.V_0(j)
+                if (j < n) {
+                    if (!(ok = wait_full(posK, 11))) break;
+                    issue_s<NQ>(p, sm, tmem, st, 0, j, ring(posK));
+                    issued_any = true;
+                    ptx::mma_commit(sm.bar(C::BAR_EMPTY + stage_of(posK)));
+                    if (j == n - 1) ptx::mma_commit(sm.bar(C::BAR_QFREE));
+                    if (!(ok = wait_full(posV, 13))) break;
+                    if (!(ok = issue_pv<NQ>(p, sm, tmem, st, 0, j, ring(posV)))) break;
+                    ptx::mma_commit(sm.bar(C::BAR_EMPTY + stage_of(posV)));
+                }
+            } else {
+                // NQ == 1, S double-buffered: S(j), P.V(j-1). S(t) waits until the
+                // softmax has read S(t-1), so S-full never runs two phases ahead.
+                if (j < n) {
+                    if (!(ok = wait_full(posK, 11))) break;
+                    const uint32_t t = st.jt[0] + j;
+                    if (t > 0 && !ptx::mbar_wait(sm.gbar(0, SFREE), (t - 1) & 1u, lim, abort)) {
                         ok = false;
                         record_timeout(p, abort, 12);
                         break;
                     }
-                    issue_s<NQ>(p, sm, tmem, st, x, j, ring(posK));
+                    issue_s<NQ>(p, sm, tmem, st, 0, j, ring(posK));
                     issued_any = true;
                     ptx::mma_commit(sm.bar(C::BAR_EMPTY + stage_of(posK)));
                     if (j == n - 1) ptx::mma_commit(sm.bar(C::BAR_QFREE));
                 }
                 if (j > 0) {
                     if (!(ok = wait_full(posVp, 13))) break;
-                    if (!(ok = issue_pv<NQ>(p, sm, tmem, st, x, j - 1, ring(posVp)))) break;
+                    if (!(ok = issue_pv<NQ>(p, sm, tmem, st, 0, j - 1, ring(posVp)))) break;
                     ptx::mma_commit(sm.bar(C::BAR_EMPTY + stage_of(posVp)));
                 }
             }
         }
         st.it0 += 2u * n;
-        st.jt += n;
-        ++st.kx;
+        st.jt[0] += n;
+        ++st.kx[0];
+        if (NQ == 2 && nq == 2) {  // static indices keep the counters in registers
+            st.jt[NQ - 1] += n;
+            ++st.kx[NQ - 1];
+        }
         ++k;
     }
     if (!ok && issued_any) {
-        ptx::mma_commit(sm.bar(C::BAR_DRAIN + x));
-        ptx::mbar_wait(sm.bar(C::BAR_DRAIN + x), 0, lim, nullptr);
+        ptx::mma_commit(sm.bar(C::BAR_DRAIN));
+        ptx::mbar_wait(sm.bar(C::BAR_DRAIN), 0, lim, nullptr);
     }
 }
 
@@ -459,7 +426,7 @@ __device__ void softmax_group(const SplitParams& p, const Smem<NQ>& sm, uint32_t
     bool ok = true;
     for (int ui = p.cta_first[blockIdx.x]; ui < p.cta_first[blockIdx.x + 1] && ok; ++ui) {
         const Unit u = p.units[ui];
-        const int n_tiles = unit_tiles<NQ>(u);
+        const int n_tiles = unit_tiles(u);
         if (n_tiles <= 0 || x >= unit_nq<NQ>(u, p.tpt)) continue;
         const int urow = kBM * x + row;  // row within the unit
         const bool row_valid = urow < u.n_tok * p.G;
@@ -469,7 +436,7 @@ __device__ void softmax_group(const SplitParams& p, const Smem<NQ>& sm, uint32_t
         const int vis_end = row_valid ? min(u.key_end, u.pos_base + tok + 1) : 0;
         float m_ref = -INFINITY, l_run = 0.f;
         for (int j = 0; j < n_tiles; ++j, ++jt) {
-            const int kt = u.key_begin + j * C::kBN;
+            const int kt = u.key_begin + j * kBN;
             bool w = ptx::mbar_wait(sm.gbar(x, SFULL), jt & 1u, lim, abort);
             if (!__all_sync(0xffffffffu, w)) { ok = false; record_timeout(p, abort, 20); break; }
             ptx::tc_fence_after();
@@ -482,29 +449,28 @@ __device__ void softmax_group(const SplitParams& p, const Smem<NQ>& sm, uint32_t
             float corr = 1.f;
             if (active) {
                 const int lim_c = vis_end - kt;
-                constexpr int BN = C::kBN;
-                const bool full = __all_sync(0xffffffffu, lim_c >= BN);
-                uint32_t s[BN];
+                const bool full = __all_sync(0xffffffffu, lim_c >= kBN);
+                uint32_t s[kBN];
 #pragma unroll
-                for (int c = 0; c < BN / 32; ++c) {
+                for (int c = 0; c < 4; ++c) {
                     uint32_t (&chunk)[32] = *reinterpret_cast<uint32_t (*)[32]>(&s[32 * c]);
                     ptx::tmem_ld32(lane_addr + colS + 32 * c, chunk);
                 }
 #pragma unroll
-                for (int c = 0; c < BN / 32; ++c) {
+                for (int c = 0; c < 4; ++c) {
                     uint32_t (&chunk)[32] = *reinterpret_cast<uint32_t (*)[32]>(&s[32 * c]);
                     if (c == 0) ptx::tmem_ld_wait(chunk); else ptx::reg_touch(chunk);
                 }
                 if (!full) {
 #pragma unroll
-                    for (int c = 0; c < BN; ++c)
+                    for (int c = 0; c < kBN; ++c)
                         if (c >= lim_c) s[c] = __float_as_uint(-INFINITY);
                 }
                 float mx[8];
 #pragma unroll
                 for (int q = 0; q < 8; ++q) mx[q] = -INFINITY;
 #pragma unroll
-                for (int c = 0; c < BN; c += 2)  // three-input max: two columns per step
+                for (int c = 0; c < kBN; c += 2)  // three-input max: two columns per step
                     mx[(c >> 1) & 7] = ptx::fmax3(mx[(c >> 1) & 7], __uint_as_float(s[c]),
                                                   __uint_as_float(s[c + 1]));
                 const float mt = max8(mx) * sl2;  // scale > 0: max commutes with scaling
@@ -517,16 +483,16 @@ __device__ void softmax_group(const SplitParams& p, const Smem<NQ>& sm, uint32_t
 #pragma unroll
                 for (int q = 0; q < 8; ++q) sm8[q] = 0.f;
 #pragma unroll
-                for (int c = 0; c < BN; ++c) {
+                for (int c = 0; c < kBN; ++c) {
                     const float e = ptx::ex2(fmaf(__uint_as_float(s[c]), sl2, -m_use));
                     s[c] = __float_as_uint(e);
                     sm8[c & 7] += e;
                 }
 #pragma unroll
-                for (int i = 0; i < BN / 2; ++i)
+                for (int i = 0; i < 64; ++i)
                     s[i] = ptx::pack_bf16x2(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1]));
 #pragma unroll
-                for (int c = 0; c < BN / 64; ++c) {
+                for (int c = 0; c < 2; ++c) {
                     uint32_t (&chunk)[32] = *reinterpret_cast<uint32_t (*)[32]>(&s[32 * c]);
                     ptx::tmem_st32(lane_addr + colS + 32 * c, chunk);
                 }
@@ -535,11 +501,11 @@ __device__ void softmax_group(const SplitParams& p, const Smem<NQ>& sm, uint32_t
             }
             // The previous P.V must be done before O is rescaled in place. With one
             // query tile the wait comes every tile: it also keeps P-full from
-            // running two phases ahead of the issuer (S of the next tile does not
-            // wait for P.V). With two, S_x(j+1) follows P_x.V(j), so only a rescale
-            // needs it; the P.V is normally complete already.
+            // running two phases ahead of the MMA thread (S of the next tile does
+            // not wait for P.V). With two, S_x(j) is issued after P_x.V(j-1), so
+            // S-full already implies that P.V completed: no wait is needed.
             const bool rescale = j > 0 && __any_sync(0xffffffffu, corr != 1.f);
-            if (j > 0 && (NQ == 1 || rescale)) {
+            if (NQ == 1 && j > 0) {
                 w = ptx::mbar_wait(sm.gbar(x, ODONE), (jt - 1) & 1u, lim, abort);
                 if (!__all_sync(0xffffffffu, w)) { ok = false; record_timeout(p, abort, 21); break; }
                 ptx::tc_fence_after();
@@ -840,12 +806,12 @@ __global__ void __launch_bounds__(Cfg<NQ>::kThreads, 1) __maxnreg__(NQ == 2 ? 20
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
             ptx::mbar_init(sm.bar(C::BAR_FULL + s), 1);
-            ptx::mbar_init(sm.bar(C::BAR_EMPTY + s), NQ);  // one commit per issuer
+            ptx::mbar_init(sm.bar(C::BAR_EMPTY + s), 1);
         }
         ptx::mbar_init(sm.bar(C::BAR_QFULL), 1);
-        ptx::mbar_init(sm.bar(C::BAR_QFREE), NQ);
+        ptx::mbar_init(sm.bar(C::BAR_QFREE), 1);
         ptx::mbar_init(sm.bar(C::BAR_AUX), 1);
-        for (int x = 0; x < NQ; ++x) ptx::mbar_init(sm.bar(C::BAR_DRAIN + x), 1);
+        ptx::mbar_init(sm.bar(C::BAR_DRAIN), 1);
         for (int x = 0; x < NQ; ++x) {
             ptx::mbar_init(sm.gbar(x, SFULL), 1);
             ptx::mbar_init(sm.gbar(x, PFULL), 128);
@@ -873,11 +839,11 @@ __global__ void __launch_bounds__(Cfg<NQ>::kThreads, 1) __maxnreg__(NQ == 2 ? 20
 
     if (warp == 0) {
         producer_warp<NQ>(p, sm, &tm_q, &tm_k, &tm_v);
-    } else if (warp < C::kSoftmaxWarp0) {
-        if (lane == 0) mma_thread<NQ>(p, sm, tmem, warp - 1);
+    } else if (warp == 1) {
+        if (lane == 0) mma_thread<NQ>(p, sm, tmem);
         __syncwarp();
     } else {
-        softmax_group<NQ>(p, sm, tmem, (warp - C::kSoftmaxWarp0) >> 2);
+        softmax_group<NQ>(p, sm, tmem, (warp - 2) >> 2);
     }
 
     ptx::tc_fence_before();

@@ -10,9 +10,7 @@
 namespace fanout {
 
 constexpr int kBM = 128;      // query rows per tile (tcgen05 M)
-constexpr int kBN = 128;      // keys per planning tile (the planner's unit of work)
-// Keys per K/V tile of the attention kernel for a plan with nq query tiles per unit.
-constexpr int kv_tile_keys(int /*nq*/) { return 128; }
+constexpr int kBN = 128;      // keys per KV tile
 constexpr int kHD = 128;      // head dimension handled by this build
 constexpr int kNoCausal = 1 << 30;  // pos_base for units that need no causal mask
 

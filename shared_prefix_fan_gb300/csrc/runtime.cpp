@@ -37,8 +37,7 @@ int status_of(cudaError_t e) {
 }
 
 // K / V page pool viewed as [num_pages * H_kv * page][128] bf16; a box is one
-// page of one KV head (or a K/V tile's rows of it, when pages are larger than
-// the kernel's tile), 64 columns (128 bytes, the swizzle span) wide.
+// page of one KV head, 64 columns (128 bytes, the swizzle span) wide.
 int map_pool(CUtensorMap* m, const void* base, int64_t rows, int32_t box_rows) {
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHD), static_cast<cuuint64_t>(rows)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHD) * 2};
@@ -154,9 +153,8 @@ int launch_plan(const CallArgs& a, const Plan& pl, const Layout& L, uint8_t* bas
     const int64_t pool_rows = static_cast<int64_t>(a.num_pages) * a.H_kv * a.page_size;
     int st;
     if ((st = map_q(&tm_q, a.q, a.R, a.H_q, G, pl.tpt)) != FANOUT_OK) return st;
-    const int32_t box_rows = std::min<int32_t>(a.page_size, kv_tile_keys(pl.nq));
-    if ((st = map_pool(&tm_k, a.k, pool_rows, box_rows)) != FANOUT_OK) return st;
-    if ((st = map_pool(&tm_v, a.v, pool_rows, box_rows)) != FANOUT_OK) return st;
+    if ((st = map_pool(&tm_k, a.k, pool_rows, a.page_size)) != FANOUT_OK) return st;
+    if ((st = map_pool(&tm_v, a.v, pool_rows, a.page_size)) != FANOUT_OK) return st;
     int32_t* err = nullptr;
     cudaError_t ce = err_word_ptr(&err);
     if (ce != cudaSuccess) return status_of(ce);
