@@ -248,6 +248,25 @@ __device__ void producer_warp(const SplitParams& p, const Smem<NQ>& sm, const CU
     }
 }
 
+// Warm L1 with the first unit of this CTA and the first 32 page ids of its
+// range (a chain of three dependent global reads the producer would otherwise
+// start only after the set-up barrier). Run by an idle warp at kernel entry.
+template <int NQ>
+__device__ __forceinline__ void warm_first_unit(const SplitParams& p, const Smem<NQ>& sm) {
+    const int lane = threadIdx.x & 31;
+    const int u0 = p.cta_first[blockIdx.x];
+    if (u0 >= p.cta_first[blockIdx.x + 1]) return;
+    const Unit u = p.units[u0];
+    const int ps = p.page_size;
+    const int n_pages = (u.key_end - u.key_begin + ps - 1) / ps;
+    int v = 0;
+    if (lane < n_pages)
+        v = __ldg(p.page_table + static_cast<int64_t>(u.branch) * p.max_pages + u.key_begin / ps +
+                  lane);
+    // keep the loads: a store no one reads, taken only for an impossible value
+    if (__any_sync(0xffffffffu, v == INT32_MIN)) *sm.merge_go() = v;
+}
+
 // ------------------------------------------------------------------ MMA issuer
 __device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile_base, int kk) {
     // K-major, 128-byte swizzle: 64-column halves 16 KB apart, 8-row groups 1 KB
@@ -661,6 +680,73 @@ __device__ __noinline__ int merge_chunk_index(const MergeParams& mp, int64_t n, 
     return rows;
 }
 
+// Folds the rows of a warp's chunk from shared memory and writes out / lse.
+// dry: the same instructions on whatever the slots hold, results kept in
+// shared memory -- run while the other CTAs finish, it brings this code into
+// the instruction cache (after an L2 flush, a cold fetch of the fold costs
+// microseconds on the critical path of the last CTA).
+template <int NQ>
+__device__ __noinline__ void merge_fold_chunk(const MergeParams& mp, int64_t n, int rows,
+                                              uint8_t* region, int lane, bool dry) {
+    using M = MergeStage<NQ>;
+    float* so = reinterpret_cast<float*>(region);
+    const float2* sml = reinterpret_cast<const float2*>(region + M::kSlots * 520);
+    const int* tne = reinterpret_cast<const int*>(region + M::kSlots * 528 + kChunkRows * 8);
+    const int* tfirst = tne + kChunkRows;
+    const int kb = (mp.merge_stride <= 8) ? 8 : 24;  // the pass size merge_row uses
+    for (int k = 0; k < rows; ++k) {
+        const int64_t nk = n + static_cast<int64_t>(k) * M::kWarps;
+        const int c = tne[k];
+        if (c == 0) continue;
+        if (c < 0) {
+            if (!dry) merge_row<24>(mp, nk, lane);
+            continue;
+        }
+        const int f = tfirst[k];
+        float Mx = -INFINITY, L = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int c0 = 0; c0 < c; c0 += kb) {
+            const int cnt = min(kb, c - c0);
+            const float2 ml = (lane < cnt) ? sml[f + c0 + lane] : make_float2(-INFINITY, 0.f);
+            float mb = (ml.y > 0.f) ? ml.x : -INFINITY;
+            for (int s = 16; s > 0; s >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, s));
+            const float m_new = fmaxf(Mx, mb);
+            const float corr = (Mx == -INFINITY) ? 0.f : ptx::ex2(Mx - m_new);
+            const float w = (ml.y > 0.f) ? ptx::ex2(ml.x - m_new) : 0.f;
+            float lb = w * ml.y;
+            for (int s = 16; s > 0; s >>= 1) lb += __shfl_xor_sync(0xffffffffu, lb, s);
+            L = L * corr + lb;
+            acc.x *= corr;
+            acc.y *= corr;
+            acc.z *= corr;
+            acc.w *= corr;
+            for (int u = 0; u < cnt; ++u) {
+                const float wu = __shfl_sync(0xffffffffu, w, u);
+                const float4 o = reinterpret_cast<const float4*>(so + (f + c0 + u) * kHD)[lane];
+                acc.x += wu * o.x;
+                acc.y += wu * o.y;
+                acc.z += wu * o.z;
+                acc.w += wu * o.w;
+            }
+            Mx = m_new;
+        }
+        const float inv = 1.f / L;
+        if (dry) {
+            reinterpret_cast<float4*>(so)[lane] =
+                make_float4(acc.x * inv, acc.y * inv, acc.z * inv, Mx + __log2f(L));
+        } else if (mp.out_bf16) {
+            uint2 v = make_uint2(ptx::pack_bf16x2(acc.x * inv, acc.y * inv),
+                                 ptx::pack_bf16x2(acc.z * inv, acc.w * inv));
+            reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(mp.out) + nk * kHD)[lane] = v;
+        } else {
+            reinterpret_cast<float4*>(static_cast<float*>(mp.out) + nk * kHD)[lane] =
+                make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+        }
+        if (!dry && mp.lse && lane == 0) mp.lse[nk] = (Mx + __log2f(L)) * 0.69314718055994531f;
+    }
+    __syncwarp();
+}
+
 template <int NQ>
 __device__ __noinline__ void merge_tail(const SplitParams& p, const Smem<NQ>& sm) {
     using M = MergeStage<NQ>;
@@ -679,8 +765,7 @@ __device__ __noinline__ void merge_tail(const SplitParams& p, const Smem<NQ>& sm
     const int64_t r1 = min(n_out, r0 + per);
     uint8_t* region = sm.ptr + warp * M::kRegion;
     const uint32_t region_s = sm.base + warp * M::kRegion;
-    const float* so = reinterpret_cast<const float*>(region);
-    int64_t* sidx = reinterpret_cast<int64_t*>(region + M::kSlots * 512);
+    const int64_t* sidx = reinterpret_cast<const int64_t*>(region + M::kSlots * 512);
     float2* sml = reinterpret_cast<float2*>(region + M::kSlots * 520);
     const int* tne = reinterpret_cast<const int*>(region + M::kSlots * 528 + kChunkRows * 8);
     const int* tfirst = tne + kChunkRows;
@@ -689,6 +774,9 @@ __device__ __noinline__ void merge_tail(const SplitParams& p, const Smem<NQ>& sm
     ptx::fence_proxy_async_smem();
     int64_t n = r0 + warp;
     int rows = (n < r1) ? merge_chunk_index<NQ>(mp, n, r1, region, lane) : 0;
+    // While the other CTAs finish: a dry fold of the first chunk (instruction
+    // cache), then the wait for every CTA's flag.
+    if (rows > 0) merge_fold_chunk<NQ>(mp, n, rows, region, lane, true);
 
     if (warp == 0) {
         bool all = false;
@@ -705,7 +793,7 @@ __device__ __noinline__ void merge_tail(const SplitParams& p, const Smem<NQ>& sm
             }
             if (ptx::globaltimer_ns() - t0 > p.wait_limit_ns) break;
         }
-        __threadfence();  // every lane: acquire side of the flags it read
+        __threadfence();  // acquire side of the flags; the barrier below extends it to the CTA
         if (lane == 0) {
             if (!all && atomicCAS(p.err, 0, kErrTimeout) == 0) {
                 p.err[1] = 30;
@@ -716,68 +804,19 @@ __device__ __noinline__ void merge_tail(const SplitParams& p, const Smem<NQ>& sm
     }
     __syncthreads();
     if (!*sm.merge_go()) return;
-    __threadfence();  // this thread's reads below come after the grid's partial writes
-    const int kb = (mp.merge_stride <= 8) ? 8 : 24;  // the pass size merge_row uses
     while (rows > 0) {
         int nslot = 0;
         for (int k = 0; k < rows; ++k)
             if (tne[k] > 0) nslot = tfirst[k] + tne[k];
+        for (int s2 = 0; s2 < nslot; ++s2)  // every O row in flight first
+            ptx::cp_async_16(region_s + s2 * 512 + lane * 16, mp.part_o + sidx[s2] * kHD + lane * 4);
         for (int s2 = lane; s2 < nslot; s2 += 32) {  // (m, l) through L2 into shared
             const float2 v = __ldcg(mp.part_ml + sidx[s2]);
             sml[s2] = v;
         }
-        for (int s2 = 0; s2 < nslot; ++s2)
-            ptx::cp_async_16(region_s + s2 * 512 + lane * 16, mp.part_o + sidx[s2] * kHD + lane * 4);
         ptx::cp_async_wait_all();
         __syncwarp();
-        for (int k = 0; k < rows; ++k) {
-            const int64_t nk = n + static_cast<int64_t>(k) * M::kWarps;
-            const int c = tne[k];
-            if (c == 0) continue;
-            if (c < 0) {
-                merge_row<24>(mp, nk, lane);
-                continue;
-            }
-            const int f = tfirst[k];
-            float Mx = -INFINITY, L = 0.f;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int c0 = 0; c0 < c; c0 += kb) {
-                const int cnt = min(kb, c - c0);
-                const float2 ml = (lane < cnt) ? sml[f + c0 + lane] : make_float2(-INFINITY, 0.f);
-                float mb = (ml.y > 0.f) ? ml.x : -INFINITY;
-                for (int s = 16; s > 0; s >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, s));
-                const float m_new = fmaxf(Mx, mb);
-                const float corr = (Mx == -INFINITY) ? 0.f : ptx::ex2(Mx - m_new);
-                const float w = (ml.y > 0.f) ? ptx::ex2(ml.x - m_new) : 0.f;
-                float lb = w * ml.y;
-                for (int s = 16; s > 0; s >>= 1) lb += __shfl_xor_sync(0xffffffffu, lb, s);
-                L = L * corr + lb;
-                acc.x *= corr;
-                acc.y *= corr;
-                acc.z *= corr;
-                acc.w *= corr;
-                for (int u = 0; u < cnt; ++u) {
-                    const float wu = __shfl_sync(0xffffffffu, w, u);
-                    const float4 o = reinterpret_cast<const float4*>(so + (f + c0 + u) * kHD)[lane];
-                    acc.x += wu * o.x;
-                    acc.y += wu * o.y;
-                    acc.z += wu * o.z;
-                    acc.w += wu * o.w;
-                }
-                Mx = m_new;
-            }
-            const float inv = 1.f / L;
-            if (mp.out_bf16) {
-                uint2 v = make_uint2(ptx::pack_bf16x2(acc.x * inv, acc.y * inv),
-                                     ptx::pack_bf16x2(acc.z * inv, acc.w * inv));
-                reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(mp.out) + nk * kHD)[lane] = v;
-            } else {
-                reinterpret_cast<float4*>(static_cast<float*>(mp.out) + nk * kHD)[lane] =
-                    make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-            }
-            if (mp.lse && lane == 0) mp.lse[nk] = (Mx + __log2f(L)) * 0.69314718055994531f;
-        }
-        __syncwarp();  // the slots are read before the next chunk overwrites them
+        merge_fold_chunk<NQ>(mp, n, rows, region, lane, false);  // ends with __syncwarp
         n += static_cast<int64_t>(rows) * M::kWarps;
         rows = (n < r1) ? merge_chunk_index<NQ>(mp, n, r1, region, lane) : 0;
     }
@@ -823,6 +862,7 @@ __global__ void __launch_bounds__(Cfg<NQ>::kThreads, 1) __maxnreg__(NQ == 2 ? 20
         ptx::fence_barrier_init();
         ptx::fence_proxy_async_smem();
     }
+    if (warp == C::kThreads / 32 - 1) warm_first_unit<NQ>(p, sm);  // a softmax warp, idle now
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tmap(&tm_q);
         ptx::prefetch_tmap(&tm_k);
