@@ -248,25 +248,6 @@ __device__ void producer_warp(const SplitParams& p, const Smem<NQ>& sm, const CU
     }
 }
 
-// Warm L1 with the first unit of this CTA and the first 32 page ids of its
-// range (a chain of three dependent global reads the producer would otherwise
-// start only after the set-up barrier). Run by an idle warp at kernel entry.
-template <int NQ>
-__device__ __forceinline__ void warm_first_unit(const SplitParams& p, const Smem<NQ>& sm) {
-    const int lane = threadIdx.x & 31;
-    const int u0 = p.cta_first[blockIdx.x];
-    if (u0 >= p.cta_first[blockIdx.x + 1]) return;
-    const Unit u = p.units[u0];
-    const int ps = p.page_size;
-    const int n_pages = (u.key_end - u.key_begin + ps - 1) / ps;
-    int v = 0;
-    if (lane < n_pages)
-        v = __ldg(p.page_table + static_cast<int64_t>(u.branch) * p.max_pages + u.key_begin / ps +
-                  lane);
-    // keep the loads: a store no one reads, taken only for an impossible value
-    if (__any_sync(0xffffffffu, v == INT32_MIN)) *sm.merge_go() = v;
-}
-
 // ------------------------------------------------------------------ MMA issuer
 __device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile_base, int kk) {
     // K-major, 128-byte swizzle: 64-column halves 16 KB apart, 8-row groups 1 KB
@@ -680,19 +661,34 @@ __device__ __noinline__ int merge_chunk_index(const MergeParams& mp, int64_t n, 
     return rows;
 }
 
-// Folds the rows of a warp's chunk from shared memory and writes out / lse.
-// dry: the same instructions on whatever the slots hold, results kept in
-// shared memory -- run while the other CTAs finish, it brings this code into
-// the instruction cache (after an L2 flush, a cold fetch of the fold costs
-// microseconds on the critical path of the last CTA).
+// Pulls a warp's chunk of partials into its slots (cp.async for the O rows,
+// every one in flight before the (m, l) loads), folds each row from shared
+// memory and writes out / lse. dry: the same instructions, but the results stay
+// in shared memory -- run while the other CTAs finish (reading partials that
+// may not be final, which is harmless), it brings this code into the
+// instruction cache: after an L2 flush a cold fetch of it costs microseconds
+// on the critical path of the last CTA.
 template <int NQ>
-__device__ __noinline__ void merge_fold_chunk(const MergeParams& mp, int64_t n, int rows,
-                                              uint8_t* region, int lane, bool dry) {
+__device__ __noinline__ void merge_chunk_run(const MergeParams& mp, int64_t n, int rows,
+                                             uint8_t* region, uint32_t region_s, int lane,
+                                             bool dry) {
     using M = MergeStage<NQ>;
     float* so = reinterpret_cast<float*>(region);
-    const float2* sml = reinterpret_cast<const float2*>(region + M::kSlots * 520);
+    const int64_t* sidx = reinterpret_cast<const int64_t*>(region + M::kSlots * 512);
+    float2* sml = reinterpret_cast<float2*>(region + M::kSlots * 520);
     const int* tne = reinterpret_cast<const int*>(region + M::kSlots * 528 + kChunkRows * 8);
     const int* tfirst = tne + kChunkRows;
+    int nslot = 0;
+    for (int k = 0; k < rows; ++k)
+        if (tne[k] > 0) nslot = tfirst[k] + tne[k];
+    for (int s2 = 0; s2 < nslot; ++s2)
+        ptx::cp_async_16(region_s + s2 * 512 + lane * 16, mp.part_o + sidx[s2] * kHD + lane * 4);
+    for (int s2 = lane; s2 < nslot; s2 += 32) {  // (m, l) through L2 into shared
+        const float2 v = __ldcg(mp.part_ml + sidx[s2]);
+        sml[s2] = v;
+    }
+    ptx::cp_async_wait_all();
+    __syncwarp();
     const int kb = (mp.merge_stride <= 8) ? 8 : 24;  // the pass size merge_row uses
     for (int k = 0; k < rows; ++k) {
         const int64_t nk = n + static_cast<int64_t>(k) * M::kWarps;
@@ -765,18 +761,14 @@ __device__ __noinline__ void merge_tail(const SplitParams& p, const Smem<NQ>& sm
     const int64_t r1 = min(n_out, r0 + per);
     uint8_t* region = sm.ptr + warp * M::kRegion;
     const uint32_t region_s = sm.base + warp * M::kRegion;
-    const int64_t* sidx = reinterpret_cast<const int64_t*>(region + M::kSlots * 512);
-    float2* sml = reinterpret_cast<float2*>(region + M::kSlots * 520);
-    const int* tne = reinterpret_cast<const int*>(region + M::kSlots * 528 + kChunkRows * 8);
-    const int* tfirst = tne + kChunkRows;
     // Every role is done and every MMA / TMA of this CTA has completed: the
     // ring is free. Order its last async-proxy use before the writes below.
     ptx::fence_proxy_async_smem();
     int64_t n = r0 + warp;
     int rows = (n < r1) ? merge_chunk_index<NQ>(mp, n, r1, region, lane) : 0;
-    // While the other CTAs finish: a dry fold of the first chunk (instruction
+    // While the other CTAs finish: a dry run of the first chunk (instruction
     // cache), then the wait for every CTA's flag.
-    if (rows > 0) merge_fold_chunk<NQ>(mp, n, rows, region, lane, true);
+    if (rows > 0) merge_chunk_run<NQ>(mp, n, rows, region, region_s, lane, true);
 
     if (warp == 0) {
         bool all = false;
@@ -805,18 +797,7 @@ __device__ __noinline__ void merge_tail(const SplitParams& p, const Smem<NQ>& sm
     __syncthreads();
     if (!*sm.merge_go()) return;
     while (rows > 0) {
-        int nslot = 0;
-        for (int k = 0; k < rows; ++k)
-            if (tne[k] > 0) nslot = tfirst[k] + tne[k];
-        for (int s2 = 0; s2 < nslot; ++s2)  // every O row in flight first
-            ptx::cp_async_16(region_s + s2 * 512 + lane * 16, mp.part_o + sidx[s2] * kHD + lane * 4);
-        for (int s2 = lane; s2 < nslot; s2 += 32) {  // (m, l) through L2 into shared
-            const float2 v = __ldcg(mp.part_ml + sidx[s2]);
-            sml[s2] = v;
-        }
-        ptx::cp_async_wait_all();
-        __syncwarp();
-        merge_fold_chunk<NQ>(mp, n, rows, region, lane, false);  // ends with __syncwarp
+        merge_chunk_run<NQ>(mp, n, rows, region, region_s, lane, false);  // ends with __syncwarp
         n += static_cast<int64_t>(rows) * M::kWarps;
         rows = (n < r1) ? merge_chunk_index<NQ>(mp, n, r1, region, lane) : 0;
     }
@@ -862,7 +843,6 @@ __global__ void __launch_bounds__(Cfg<NQ>::kThreads, 1) __maxnreg__(NQ == 2 ? 20
         ptx::fence_barrier_init();
         ptx::fence_proxy_async_smem();
     }
-    if (warp == C::kThreads / 32 - 1) warm_first_unit<NQ>(p, sm);  // a softmax warp, idle now
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tmap(&tm_q);
         ptx::prefetch_tmap(&tm_k);
