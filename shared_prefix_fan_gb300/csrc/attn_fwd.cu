@@ -766,9 +766,16 @@ __device__ __noinline__ void merge_tail(const SplitParams& p, const Smem<NQ>& sm
     ptx::fence_proxy_async_smem();
     int64_t n = r0 + warp;
     int rows = (n < r1) ? merge_chunk_index<NQ>(mp, n, r1, region, lane) : 0;
-    // While the other CTAs finish: a dry run of the first chunk (instruction
-    // cache), then the wait for every CTA's flag.
-    if (rows > 0) merge_chunk_run<NQ>(mp, n, rows, region, region_s, lane, true);
+    // While other CTAs are still working, warp 1 makes a dry run of its first
+    // chunk (instruction cache, and L2 for the CTAs that finish last); a CTA
+    // that finds almost every flag set already skips it.
+    if (warp == 1 && rows > 0) {
+        int unset = 0;
+        for (int c = lane; c < static_cast<int>(gridDim.x); c += 32)
+            unset += ptx::ld_relaxed_gpu(p.flags + c) != p.epoch;
+        for (int s = 16; s > 0; s >>= 1) unset += __shfl_xor_sync(0xffffffffu, unset, s);
+        if (unset > 8) merge_chunk_run<NQ>(mp, n, rows, region, region_s, lane, true);
+    }
 
     if (warp == 0) {
         bool all = false;
