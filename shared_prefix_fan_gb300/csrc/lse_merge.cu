@@ -19,18 +19,28 @@ __device__ int32_t g_err_word[4];
 namespace {
 
 // One warp per output row; kMergeBatch partials per pass: 24 for rows with
-// many partials (decode), 8 when every row has few (a smaller register
-// footprint keeps three blocks per SM).
-template <int kMergeBatch, int kMinBlocks>
-__global__ void __launch_bounds__(256, kMinBlocks) lse_merge_kernel(const MergeParams p) {
-    // Launched as a programmatic dependent of the attention kernel: wait until
-    // that grid has completed and its writes are visible.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+// many partials (decode), 8 when every row has few. Blocks of two warps: small
+// enough to be resident beside an attention CTA (which leaves ~27 K registers
+// and 2 KB of shared memory of an SM free), so the grid starts, and runs its
+// dry pass, while the attention kernel is still working.
+constexpr int kMergeThreads = 64;
+template <int kMergeBatch>
+__global__ void __launch_bounds__(kMergeThreads, 1) lse_merge_kernel(const MergeParams p) {
+    // Launched as a programmatic dependent of the attention kernel: this grid
+    // is resident while that one runs. Before waiting for it to complete, each
+    // warp reads its first row's merge index and makes a dry run of the row
+    // (instruction and data caches warm, nothing written).
     const int lane = threadIdx.x & 31;
     const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
-    for (int64_t n = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-         n < p.n_out; n += warps)
-        merge_row<kMergeBatch>(p, n, lane);
+    const int64_t n0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    MergeIdx ix{0, 0, 0, make_int2(0, 0)};
+    if (n0 < p.n_out) {
+        ix = merge_index(p, n0, lane);
+        merge_row_ix<kMergeBatch>(p, n0, ix, lane, true);
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (n0 < p.n_out) merge_row_ix<kMergeBatch>(p, n0, ix, lane);
+    for (int64_t n = n0 + warps; n < p.n_out; n += warps) merge_row<kMergeBatch>(p, n, lane);
 }
 
 // One thread waits on a barrier that nothing will ever complete; the bounded
@@ -52,15 +62,16 @@ cudaError_t launch_lse_merge(const MergeParams& p, cudaStream_t stream) {
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int64_t blocks_needed = (p.n_out + 7) / 8;
+    const int64_t rows_per_block = kMergeThreads / 32;
+    const int64_t blocks_needed = (p.n_out + rows_per_block - 1) / rows_per_block;
     const int grid =
-        static_cast<int>(std::min<int64_t>(blocks_needed, static_cast<int64_t>(sms) * 16));
+        static_cast<int>(std::min<int64_t>(blocks_needed, static_cast<int64_t>(sms) * 32));
     // Programmatic dependent launch: the merge grid may start while the
     // attention kernel finishes; griddepcontrol.wait orders the reads.
     const int32_t most = p.merge_cnt ? p.merge_stride : p.n_parts;  // partials of the fullest row
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(256);
+    cfg.blockDim = dim3(kMergeThreads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -68,8 +79,8 @@ cudaError_t launch_lse_merge(const MergeParams& p, cudaStream_t stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (most <= 8) return cudaLaunchKernelEx(&cfg, lse_merge_kernel<8, 3>, p);
-    return cudaLaunchKernelEx(&cfg, lse_merge_kernel<24, 1>, p);
+    if (most <= 8) return cudaLaunchKernelEx(&cfg, lse_merge_kernel<8>, p);
+    return cudaLaunchKernelEx(&cfg, lse_merge_kernel<24>, p);
 }
 
 // Device address of this device's error word (the symbol's host-side name is

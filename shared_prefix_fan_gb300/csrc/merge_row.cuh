@@ -53,9 +53,12 @@ __device__ __forceinline__ MergeIdx merge_index(const MergeParams& p, int64_t n,
 // decide anything before all loads are issued. Partials are read through L2
 // (ld.global.cg): in the fused path they were written by other SMs of the
 // same grid.
+// dry: the same work with nothing written (the result only decides a store
+// that cannot happen): run before the partials are final, it brings the code
+// and the merge index into the caches.
 template <int kBatch>
 __device__ __forceinline__ void merge_row_ix(const MergeParams& p, int64_t n,
-                                             const MergeIdx& ix, int lane) {
+                                             const MergeIdx& ix, int lane, bool dry = false) {
     const bool planned = p.merge_cnt != nullptr;
     const int32_t ne = ix.ne;
     if (ne <= 0) return;  // written directly by the attention kernel
@@ -111,6 +114,11 @@ __device__ __forceinline__ void merge_row_ix(const MergeParams& p, int64_t n,
         M = m_new;
     }
     const float inv = 1.f / L;
+    if (dry) {
+        __shared__ float dry_sink;  // keeps the dry computation; nothing reads it
+        if (acc.x * inv == 1.2345e-30f) dry_sink = acc.y;
+        return;
+    }
     if (p.out_bf16) {
         uint2 v = make_uint2(ptx::pack_bf16x2(acc.x * inv, acc.y * inv),
                              ptx::pack_bf16x2(acc.z * inv, acc.w * inv));
