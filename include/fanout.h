@@ -251,9 +251,10 @@ enum fanout_option {
     FANOUT_OPT_VALIDATE_TABLE = 2,  /* 1: check page-table entries on the host each call */
     FANOUT_OPT_WAIT_LIMIT_NS = 3,   /* bound of every device-side wait (default 1e9 ns) */
     FANOUT_OPT_NUM_SMS = 4,         /* >0: plan for this many SMs instead of the device's */
-    FANOUT_OPT_FUSED_MERGE = 5      /* 1 (default): the log-sum-exp merge runs inside the
-                                       attention kernel (cooperative launch) when every CTA
-                                       fits on the device at once; 0: separate merge kernel */
+    FANOUT_OPT_FUSED_MERGE = 5      /* 0 (default): the log-sum-exp merge is a separate kernel,
+                                       a programmatic dependent of the attention kernel; 1: it
+                                       runs inside the attention kernel (cooperative launch)
+                                       when every CTA fits on the device at once */
 };
 FANOUT_API int fanout_set_option(int32_t option, int64_t value);
 

@@ -25,7 +25,7 @@ std::mutex g_mu;
 int64_t g_force_splits = 0;
 int64_t g_validate_table = 0;
 int64_t g_num_sms_override = 0;
-int64_t g_fused_merge = 1;
+int64_t g_fused_merge = 0;
 unsigned long long g_wait_limit_ns = 1000000000ull;
 cudaEvent_t g_ev_before = nullptr;
 cudaEvent_t g_ev_after = nullptr;

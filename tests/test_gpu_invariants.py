@@ -83,7 +83,7 @@ def test_fused_merge_equals_separate_merge(name):
         o_fused, l_fused = dw.run()
         o_again, l_again = dw.run()   # next epoch on the same flags
     finally:
-        binding.set_option(binding.OPT_FUSED_MERGE, 1)
+        binding.set_option(binding.OPT_FUSED_MERGE, 0)
     assert torch.equal(o_sep, o_fused) and torch.equal(l_sep, l_fused)
     assert torch.equal(o_fused, o_again) and torch.equal(l_fused, l_again)
     compare(o_fused, l_fused, *oracle_ref(w), what=name + " fused merge")
