@@ -118,6 +118,12 @@ __device__ __forceinline__ void record_timeout(const SplitParams& p, volatile in
     }
 }
 
+// A unit re-read from memory (volatile: not kept in registers from an earlier read).
+__device__ __forceinline__ Unit load_unit_volatile(const Unit* up) {
+    const volatile int32_t* v = reinterpret_cast<const volatile int32_t*>(up);
+    return Unit{v[0], v[1], v[2], v[3], v[4], v[5], v[6], v[7]};
+}
+
 __device__ __forceinline__ int unit_tiles(const Unit& u) {
     return (u.key_end - u.key_begin + kBN - 1) / kBN;
 }
@@ -431,12 +437,13 @@ __device__ void softmax_group(const SplitParams& p, const Smem<NQ>& sm, uint32_t
         const int urow = kBM * x + row;  // row within the unit
         const bool row_valid = urow < u.n_tok * p.G;
         const bool active = __any_sync(0xffffffffu, row_valid);
-        const int tok = u.tok_begin + urow / p.G;
-        const int hq = u.kv_head * p.G + urow % p.G;
-        const int vis_end = row_valid ? min(u.key_end, u.pos_base + tok + 1) : 0;
+        // Only the key start and this row's visible end stay live through the
+        // tile loop (registers); the epilogue reads the unit again.
+        const int key_begin = u.key_begin;
+        const int vis_end = row_valid ? min(u.key_end, u.pos_base + u.tok_begin + urow / p.G + 1) : 0;
         float m_ref = -INFINITY, l_run = 0.f;
         for (int j = 0; j < n_tiles; ++j, ++jt) {
-            const int kt = u.key_begin + j * kBN;
+            const int kt = key_begin + j * kBN;
             bool w = ptx::mbar_wait(sm.gbar(x, SFULL), jt & 1u, lim, abort);
             if (!__all_sync(0xffffffffu, w)) { ok = false; record_timeout(p, abort, 20); break; }
             ptx::tc_fence_after();
@@ -531,8 +538,11 @@ __device__ void softmax_group(const SplitParams& p, const Smem<NQ>& sm, uint32_t
         if (!__all_sync(0xffffffffu, w)) { ok = false; record_timeout(p, abort, 22); break; }
         ptx::tc_fence_after();
         if (active) {
+            const Unit ue = load_unit_volatile(p.units + ui);
+            const int tok = ue.tok_begin + urow / p.G;
+            const int hq = ue.kv_head * p.G + urow % p.G;
             const int64_t orow = static_cast<int64_t>(tok) * p.H_q + hq;
-            const bool direct = u.part < 0;
+            const bool direct = ue.part < 0;
             const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
@@ -558,7 +568,7 @@ __device__ void softmax_group(const SplitParams& p, const Smem<NQ>& sm, uint32_t
                 } else {
                     const float sc = direct ? inv_l : 1.f;
                     float* base = direct ? static_cast<float*>(p.out) + orow * kHD
-                                         : p.part_o + (static_cast<int64_t>(u.part) * rows_per_part +
+                                         : p.part_o + (static_cast<int64_t>(ue.part) * rows_per_part +
                                                        urow) * kHD;
                     float4* dst = reinterpret_cast<float4*>(base + 32 * c);
 #pragma unroll
@@ -573,7 +583,7 @@ __device__ void softmax_group(const SplitParams& p, const Smem<NQ>& sm, uint32_t
                 if (direct) {
                     if (p.lse) p.lse[orow] = (m_ref + __log2f(l_run)) * 0.69314718055994531f;
                 } else {
-                    p.part_ml[static_cast<int64_t>(u.part) * rows_per_part + urow] =
+                    p.part_ml[static_cast<int64_t>(ue.part) * rows_per_part + urow] =
                         make_float2(m_ref, l_run);
                 }
             }
