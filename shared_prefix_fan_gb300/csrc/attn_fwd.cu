@@ -450,7 +450,8 @@ __device__ void softmax_group(const SplitParams& p, const Smem<NQ>& sm, uint32_t
             if (NQ == 1) {
                 // S(jt) seen: the MMA may issue S(jt+1) into the other S buffer
                 // (its S-full then cannot run two phases ahead of this wait).
-                ptx::mbar_arrive(sm.gbar(x, SFREE));
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(sm.gbar(x, SFREE));
             }
             const uint32_t colS = s_col<NQ>(x, jt);
             float corr = 1.f;
@@ -530,7 +531,8 @@ __device__ void softmax_group(const SplitParams& p, const Smem<NQ>& sm, uint32_t
                 ptx::tmem_st_wait();
             }
             ptx::tc_fence_before();
-            ptx::mbar_arrive(sm.gbar(x, PFULL));
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(sm.gbar(x, PFULL));
         }
         if (!ok) break;
         // Epilogue: the last P.V done -> this row of O to global memory.
@@ -589,7 +591,8 @@ __device__ void softmax_group(const SplitParams& p, const Smem<NQ>& sm, uint32_t
             }
         }
         ptx::tc_fence_before();
-        ptx::mbar_arrive(sm.gbar(x, OFREE));
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(sm.gbar(x, OFREE));
     }
 }
 
@@ -851,10 +854,12 @@ __global__ void __launch_bounds__(Cfg<NQ>::kThreads, 1) __maxnreg__(NQ == 2 ? 20
         ptx::mbar_init(sm.bar(C::BAR_DRAIN), 1);
         for (int x = 0; x < NQ; ++x) {
             ptx::mbar_init(sm.gbar(x, SFULL), 1);
-            ptx::mbar_init(sm.gbar(x, PFULL), 128);
+            // P-full, O-free, S-free: one arrival per softmax warp (lane 0, after
+            // the warp's own TMEM traffic and a warp barrier), not 128
+            ptx::mbar_init(sm.gbar(x, PFULL), 4);
             ptx::mbar_init(sm.gbar(x, ODONE), 1);
-            ptx::mbar_init(sm.gbar(x, OFREE), 128);
-            ptx::mbar_init(sm.gbar(x, SFREE), 128);
+            ptx::mbar_init(sm.gbar(x, OFREE), 4);
+            ptx::mbar_init(sm.gbar(x, SFREE), 4);
         }
         *sm.abort_flag() = 0;
         ptx::fence_barrier_init();
