@@ -208,11 +208,13 @@ __device__ void producer_warp(const SplitParams& p, const Smem<NQ>& sm, const CU
                 const bool partial = n_valid < kBN;
                 const uint32_t bar = partial ? sm.bar(C::BAR_AUX) : sm.bar(C::BAR_FULL + stage);
                 if (lane == 0) ptx::mbar_arrive_expect_tx(bar, static_cast<uint32_t>(n_pg * ps) * 256u);
-                for (int pg = 0; pg < n_pg; ++pg) {
-                    const int page = __shfl_sync(0xffffffffu, win_cur, pg_off + pg);
-                    if (lane == 0) {
+                {
+                    // one lane per page of the tile: the tile's copies go out in two
+                    // warp instructions (lane pg holds window entry pg_off + pg)
+                    const int page = __shfl_sync(0xffffffffu, win_cur, (pg_off + lane) & 31);
+                    if (lane < n_pg) {
                         const int row = (page * p.H_kv + u.kv_head) * ps;
-                        const uint32_t off = static_cast<uint32_t>(pg * ps) * 128u;
+                        const uint32_t off = static_cast<uint32_t>(lane * ps) * 128u;
                         ptx::tma_load_2d(dst + off, tm, bar, 0, row);
                         ptx::tma_load_2d(dst + kHalfBytes + off, tm, bar, 64, row);
                     }
