@@ -262,6 +262,11 @@ __device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile_base, int kk) {
     // apart; a 16-element K step advances 32 bytes inside the swizzle atom.
     return ptx::sdesc_sw128(tile_base + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
 }
+// Start-address field increment of K step kk in a K-major tile: 64-column
+// halves 16 KB (1024 units of 16 B) apart, 32 B (2 units) per step inside one.
+__device__ __forceinline__ uint64_t kmajor_step(int kk) {
+    return static_cast<uint64_t>((kk >> 2) * (kHalfBytes >> 4) + (kk & 3) * 2);
+}
 __device__ __forceinline__ uint64_t vmn_desc(uint32_t tile_base, int kk) {
     // V as the B operand of P.V: MN-major (d contiguous), 128-byte swizzle.
     // LBO = distance between 64-column halves, SBO = between 8-key groups;
@@ -284,9 +289,11 @@ __device__ __forceinline__ bool issue_s(const SplitParams& p, const Smem<NQ>& sm
     ptx::tc_fence_after();
     const uint32_t qb = sm.base + C::kSmemQ + x * kQBytes;
     const uint32_t d = tmem + s_col<NQ>(x, st.jt[x] + j);
+    // descriptors of the K step 0; a step only moves the start address field
+    const uint64_t dq0 = kmajor_desc(qb, 0), dk0 = kmajor_desc(kb, 0);
 #pragma unroll
     for (int kk = 0; kk < kHD / 16; ++kk)
-        ptx::mma_bf16_ss(d, kmajor_desc(qb, kk), kmajor_desc(kb, kk), kIdescQK, kk > 0);
+        ptx::mma_bf16_ss(d, dq0 + kmajor_step(kk), dk0 + kmajor_step(kk), kIdescQK, kk > 0);
     ptx::mma_commit(sm.gbar(x, SFULL));
     return true;
 }
@@ -305,9 +312,10 @@ __device__ __forceinline__ bool issue_pv(const SplitParams& p, const Smem<NQ>& s
     ptx::tc_fence_after();
     const uint32_t a = tmem + s_col<NQ>(x, st.jt[x] + jj);  // P: 64 columns of bf16 pairs
     const uint32_t d = tmem + C::kColO + 128u * x;
+    const uint64_t dv0 = vmn_desc(vb, 0);  // a 16-key step adds 2 KB: 128 in the address field
 #pragma unroll
     for (int kk = 0; kk < kBN / 16; ++kk)
-        ptx::mma_bf16_ts(d, a + 8u * kk, vmn_desc(vb, kk), kIdescPV, (jj > 0 || kk > 0) ? 1u : 0u);
+        ptx::mma_bf16_ts(d, a + 8u * kk, dv0 + 128u * kk, kIdescPV, (jj > 0 || kk > 0) ? 1u : 0u);
     ptx::mma_commit(sm.gbar(x, ODONE));
     return true;
 }
