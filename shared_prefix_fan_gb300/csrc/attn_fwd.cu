@@ -497,18 +497,28 @@ __device__ void softmax_group(const SplitParams& p, const Smem<NQ>& sm, uint32_t
                     m_ref = mt;
                 }
                 const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+                // column pairs on the packed fp32x2 pipe: one FMA and one add per
+                // two columns (the exponentials stay on the MUFU, one per column);
+                // P is packed to bf16 pairs in place as the pairs are consumed
+                uint64_t sm2[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) sm2[q] = 0ull;
+                const uint64_t sl2p = ptx::f32x2(sl2, sl2), negm = ptx::f32x2(-m_use, -m_use);
+#pragma unroll
+                for (int c = 0; c < kBN; c += 2) {
+                    const uint64_t t = ptx::fma_f32x2(ptx::f32x2(__uint_as_float(s[c]),
+                                                                 __uint_as_float(s[c + 1])),
+                                                      sl2p, negm);
+                    const float e0 = ptx::ex2(ptx::lo_f32(t)), e1 = ptx::ex2(ptx::hi_f32(t));
+                    sm2[(c >> 1) & 3] = ptx::add_f32x2(sm2[(c >> 1) & 3], ptx::f32x2(e0, e1));
+                    s[c >> 1] = ptx::pack_bf16x2(e0, e1);
+                }
                 float sm8[8];
 #pragma unroll
-                for (int q = 0; q < 8; ++q) sm8[q] = 0.f;
-#pragma unroll
-                for (int c = 0; c < kBN; ++c) {
-                    const float e = ptx::ex2(fmaf(__uint_as_float(s[c]), sl2, -m_use));
-                    s[c] = __float_as_uint(e);
-                    sm8[c & 7] += e;
+                for (int q = 0; q < 4; ++q) {
+                    sm8[2 * q] = ptx::lo_f32(sm2[q]);
+                    sm8[2 * q + 1] = ptx::hi_f32(sm2[q]);
                 }
-#pragma unroll
-                for (int i = 0; i < 64; ++i)
-                    s[i] = ptx::pack_bf16x2(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1]));
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
                     uint32_t (&chunk)[32] = *reinterpret_cast<uint32_t (*)[32]>(&s[32 * c]);
