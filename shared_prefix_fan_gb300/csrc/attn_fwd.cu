@@ -65,14 +65,15 @@ struct Cfg {
     static constexpr int kSmemQ = 0;
     static constexpr int kSmemRing = kSmemQ + NQ * kQBytes;
     static constexpr int kSmemBar = kSmemRing + kStages * kTileBytes;
-    // barriers: ring full/empty, Q full/free, aux, drain, then 4 per softmax group
+    // barriers: ring full/empty, Q full/free per query tile, aux, drain, then 5
+    // per softmax group
     static constexpr int BAR_FULL = 0;
     static constexpr int BAR_EMPTY = kStages;
-    static constexpr int BAR_QFULL = 2 * kStages;
-    static constexpr int BAR_QFREE = BAR_QFULL + 1;
-    static constexpr int BAR_AUX = BAR_QFULL + 2;
-    static constexpr int BAR_DRAIN = BAR_QFULL + 3;
-    static constexpr int BAR_GROUP = BAR_QFULL + 4;  // + 5 x + {SFULL, PFULL, ODONE, OFREE, SFREE}
+    static constexpr int BAR_QFULL = 2 * kStages;  // + x
+    static constexpr int BAR_QFREE = BAR_QFULL + NQ;  // + x
+    static constexpr int BAR_AUX = BAR_QFREE + NQ;
+    static constexpr int BAR_DRAIN = BAR_AUX + 1;
+    static constexpr int BAR_GROUP = BAR_DRAIN + 1;  // + 5 x + {SFULL, PFULL, ODONE, OFREE, SFREE}
     static constexpr int kNumBars = BAR_GROUP + 5 * NQ;
     static constexpr int kSmemMisc = kSmemBar + kNumBars * 8;
     static constexpr int kSmemTotal = kSmemMisc + 16;
@@ -135,6 +136,37 @@ __device__ __forceinline__ int unit_nq(const Unit& u, int tpt) {
 }
 
 // ------------------------------------------------------------------ producer
+// Q tile x of unit u into its buffer (lane 0 of the producer warp), once the
+// buffer's previous contents were used by their last S MMA.
+template <int NQ>
+__device__ __forceinline__ bool load_q(const SplitParams& p, const Smem<NQ>& sm,
+                                       const CUtensorMap* tm_q, const Unit& u, int x,
+                                       uint32_t& loads) {
+    using C = Cfg<NQ>;
+    const int lane = threadIdx.x & 31;
+    if (loads > 0) {
+        bool w = true;
+        if (lane == 0)
+            w = ptx::mbar_wait(sm.bar(C::BAR_QFREE + x), (loads - 1) & 1u, p.wait_limit_ns,
+                               sm.abort_flag());
+        if (!__shfl_sync(0xffffffffu, w, 0)) {
+            if (lane == 0) record_timeout(p, sm.abort_flag(), 1);
+            return false;
+        }
+    }
+    if (lane == 0) {
+        const uint32_t qb = sm.bar(C::BAR_QFULL + x);
+        const int box_bytes = p.G * p.tpt * 128;  // one half of one query tile
+        ptx::mbar_arrive_expect_tx(qb, static_cast<uint32_t>(2 * box_bytes));
+        const uint32_t dst = sm.base + C::kSmemQ + x * kQBytes;
+        const int y = u.kv_head * p.G, z = u.tok_begin + x * p.tpt;
+        ptx::tma_load_3d(dst, tm_q, qb, 0, y, z);
+        ptx::tma_load_3d(dst + kHalfBytes, tm_q, qb, 64, y, z);
+    }
+    ++loads;
+    return true;
+}
+
 template <int NQ>
 __device__ void producer_warp(const SplitParams& p, const Smem<NQ>& sm, const CUtensorMap* tm_q,
                               const CUtensorMap* tm_k, const CUtensorMap* tm_v) {
@@ -143,34 +175,38 @@ __device__ void producer_warp(const SplitParams& p, const Smem<NQ>& sm, const CU
     const uint64_t lim = p.wait_limit_ns;
     volatile int* abort = sm.abort_flag();
     const int ps = p.page_size;
-    const int box_bytes = p.G * p.tpt * 128;  // one half of one query tile
     uint32_t it = 0;            // ring position
     uint32_t issued_mask = 0;   // stages ever loaded
     uint32_t issued_par = 0;    // parity of the last phase loaded per stage
     bool aux_pending = false;
     uint32_t aux_phase = 0;
+    uint32_t q_loads[NQ] = {};  // loads of each Q buffer so far
     bool ok = true;
     int k = 0;
-    for (int ui = p.cta_first[blockIdx.x]; ui < p.cta_first[blockIdx.x + 1] && ok; ++ui) {
+    const int ui_end = p.cta_first[blockIdx.x + 1];
+    for (int ui = p.cta_first[blockIdx.x]; ui < ui_end && ok; ++ui) {
         const Unit u = p.units[ui];
         const int n_tiles = unit_tiles(u);
         if (n_tiles <= 0) continue;
         const int nq = unit_nq<NQ>(u, p.tpt);
-        // Q tiles: the Q buffers are free once the previous unit's last S MMA completed.
-        if (k > 0) {
-            bool w = true;
-            if (lane == 0) w = ptx::mbar_wait(sm.bar(C::BAR_QFREE), (k - 1) & 1, lim, abort);
-            if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; if (lane == 0) record_timeout(p, abort, 1); break; }
+        // The CTA's first unit loads its Q tiles first. A later unit's Q waits
+        // for the previous unit's last S MMAs, so its first K/V tile is issued
+        // before (the ring keeps flowing across the boundary) and its Q is
+        // brought into L2 one unit ahead (the load is then an L2 hit).
+        if (k == 0) {
+#pragma unroll
+            for (int x = 0; x < NQ; ++x)
+                if (ok && x < nq) ok = load_q<NQ>(p, sm, tm_q, u, x, q_loads[x]);
         }
-        if (lane == 0) {
-            const uint32_t qb = sm.bar(C::BAR_QFULL);
-            ptx::mbar_arrive_expect_tx(qb, static_cast<uint32_t>(2 * nq * box_bytes));
-            const int y = u.kv_head * p.G;
-            for (int x = 0; x < nq; ++x) {
-                const uint32_t dst = sm.base + C::kSmemQ + x * kQBytes;
-                const int z = u.tok_begin + x * p.tpt;
-                ptx::tma_load_3d(dst, tm_q, qb, 0, y, z);
-                ptx::tma_load_3d(dst + kHalfBytes, tm_q, qb, 64, y, z);
+        if (!ok) break;
+        if (lane == 0 && ui + 1 < ui_end) {
+            const Unit un = p.units[ui + 1];
+            if (unit_tiles(un) > 0) {
+                for (int x = 0; x < unit_nq<NQ>(un, p.tpt); ++x) {
+                    const int y = un.kv_head * p.G, z = un.tok_begin + x * p.tpt;
+                    ptx::tma_prefetch_3d(tm_q, 0, y, z);
+                    ptx::tma_prefetch_3d(tm_q, 64, y, z);
+                }
             }
         }
         // Page ids of the unit, 32 per window (lane l holds page l of the window),
@@ -244,6 +280,11 @@ __device__ void producer_warp(const SplitParams& p, const Smem<NQ>& sm, const CU
                     if (lane == 0) ptx::mbar_arrive(sm.bar(C::BAR_FULL + stage));
                 }
             }
+            if (k > 0 && j == 0) {
+#pragma unroll
+                for (int x = 0; x < NQ; ++x)
+                    if (ok && x < nq) ok = load_q<NQ>(p, sm, tm_q, u, x, q_loads[x]);
+            }
         }
         ++k;
     }
@@ -253,6 +294,10 @@ __device__ void producer_warp(const SplitParams& p, const Smem<NQ>& sm, const CU
             if (issued_mask & (1u << s))
                 ptx::mbar_wait(sm.bar(C::BAR_FULL + s), (issued_par >> s) & 1u, lim, nullptr);
         if (aux_pending) ptx::mbar_wait(sm.bar(C::BAR_AUX), aux_phase, lim, nullptr);
+#pragma unroll
+        for (int x = 0; x < NQ; ++x)
+            if (q_loads[x] > 0)
+                ptx::mbar_wait(sm.bar(C::BAR_QFULL + x), (q_loads[x] - 1) & 1u, lim, nullptr);
     }
 }
 
@@ -274,61 +319,90 @@ __device__ __forceinline__ uint64_t vmn_desc(uint32_t tile_base, int kk) {
     return ptx::sdesc_sw128(tile_base + kk * 2048, kHalfBytes, 1024);
 }
 
-template <int NQ>
-struct MmaState {
-    uint32_t it0 = 0;      // ring position of the unit's K_0 (K_j at it0+2j, V_j at it0+2j+1)
-    uint32_t jt[NQ] = {};  // tiles each softmax group processed before this unit
-    int kx[NQ] = {};       // units each softmax group processed before this unit
+// One P.V product: group x's P of its t-th tile (counted over the CTA) times
+// the V tile at ring position pos. first: the unit's first product (O is
+// overwritten, and the previous unit's O of group x must have been read out:
+// kx = units group x finished before).
+struct PvOp {
+    int x;
+    uint32_t t;
+    bool first;
+    int kx;
+    uint32_t pos;
 };
 
 template <int NQ>
-__device__ __forceinline__ bool issue_s(const SplitParams& p, const Smem<NQ>& sm, uint32_t tmem,
-                                        const MmaState<NQ>& st, int x, int j, uint32_t kb) {
+__device__ __forceinline__ void issue_s(const Smem<NQ>& sm, uint32_t tmem, int x, uint32_t t,
+                                        uint32_t kb) {
     using C = Cfg<NQ>;
     // (the TMEM this S overwrites held a P whose P.V was issued earlier)
     ptx::tc_fence_after();
     const uint32_t qb = sm.base + C::kSmemQ + x * kQBytes;
-    const uint32_t d = tmem + s_col<NQ>(x, st.jt[x] + j);
+    const uint32_t d = tmem + s_col<NQ>(x, t);
     // descriptors of the K step 0; a step only moves the start address field
     const uint64_t dq0 = kmajor_desc(qb, 0), dk0 = kmajor_desc(kb, 0);
 #pragma unroll
     for (int kk = 0; kk < kHD / 16; ++kk)
         ptx::mma_bf16_ss(d, dq0 + kmajor_step(kk), dk0 + kmajor_step(kk), kIdescQK, kk > 0);
     ptx::mma_commit(sm.gbar(x, SFULL));
-    return true;
 }
 
 template <int NQ>
 __device__ __forceinline__ bool issue_pv(const SplitParams& p, const Smem<NQ>& sm, uint32_t tmem,
-                                         const MmaState<NQ>& st, int x, int jj, uint32_t vb) {
+                                         const PvOp& op, uint32_t vb) {
     using C = Cfg<NQ>;
     const uint64_t lim = p.wait_limit_ns;
     volatile int* abort = sm.abort_flag();
-    // P of tile jj written (and O rescaled) by softmax x; for the unit's first
+    // P of the tile written (and O rescaled) by softmax x; for the unit's first
     // product, the previous unit's O of group x read out.
-    if (!ptx::mbar_wait(sm.gbar(x, PFULL), (st.jt[x] + jj) & 1u, lim, abort)) { record_timeout(p, abort, 14); return false; }
-    if (jj == 0 && st.kx[x] > 0 &&
-        !ptx::mbar_wait(sm.gbar(x, OFREE), (st.kx[x] - 1) & 1, lim, abort)) { record_timeout(p, abort, 15); return false; }
+    if (!ptx::mbar_wait(sm.gbar(op.x, PFULL), op.t & 1u, lim, abort)) { record_timeout(p, abort, 14); return false; }
+    if (op.first && op.kx > 0 &&
+        !ptx::mbar_wait(sm.gbar(op.x, OFREE), (op.kx - 1) & 1, lim, abort)) { record_timeout(p, abort, 15); return false; }
     ptx::tc_fence_after();
-    const uint32_t a = tmem + s_col<NQ>(x, st.jt[x] + jj);  // P: 64 columns of bf16 pairs
-    const uint32_t d = tmem + C::kColO + 128u * x;
+    const uint32_t a = tmem + s_col<NQ>(op.x, op.t);  // P: 64 columns of bf16 pairs
+    const uint32_t d = tmem + C::kColO + 128u * op.x;
     const uint64_t dv0 = vmn_desc(vb, 0);  // a 16-key step adds 2 KB: 128 in the address field
 #pragma unroll
     for (int kk = 0; kk < kBN / 16; ++kk)
-        ptx::mma_bf16_ts(d, a + 8u * kk, dv0 + 128u * kk, kIdescPV, (jj > 0 || kk > 0) ? 1u : 0u);
-    ptx::mma_commit(sm.gbar(x, ODONE));
+        ptx::mma_bf16_ts(d, a + 8u * kk, dv0 + 128u * kk, kIdescPV, (!op.first || kk > 0) ? 1u : 0u);
+    ptx::mma_commit(sm.gbar(op.x, ODONE));
     return true;
 }
 
+// The held P.V, if any (its V stage is released once it completes).
 template <int NQ>
-__device__ void mma_thread(const SplitParams& p, const Smem<NQ>& sm, uint32_t tmem) {
+__device__ __forceinline__ bool issue_held(const SplitParams& p, const Smem<NQ>& sm, uint32_t tmem,
+                                           const PvOp& op, bool& held) {
+    using C = Cfg<NQ>;
+    if (!held) return true;
+    held = false;
+    const uint32_t stage = op.pos % C::kStages;
+    if (!ptx::mbar_wait(sm.bar(C::BAR_FULL + stage), (op.pos / C::kStages) & 1u, p.wait_limit_ns,
+                        sm.abort_flag())) {
+        record_timeout(p, sm.abort_flag(), 13);
+        return false;
+    }
+    if (!issue_pv<NQ>(p, sm, tmem, op, sm.base + C::kSmemRing + stage * kTileBytes)) return false;
+    ptx::mma_commit(sm.bar(C::BAR_EMPTY + stage));
+    return true;
+}
+
+// The single tcgen05 issuer, two query tiles per unit: per K/V tile j the
+// order S_0(j), P.V_1(j-1), S_1(j), P.V_0(j), so that one tile's softmax runs
+// while the tensor core works on the other's products (ping-pong); the unit's
+// last P.V_1 is issued before the next unit starts. Units with one query tile
+// run S_0(j), P.V_0(j).
+template <int NQ>
+__device__ void mma_thread_pair(const SplitParams& p, const Smem<NQ>& sm, uint32_t tmem) {
     using C = Cfg<NQ>;
     const uint64_t lim = p.wait_limit_ns;
     volatile int* abort = sm.abort_flag();
-    MmaState<NQ> st;
     bool ok = true;
     bool issued_any = false;
-    int k = 0;
+    uint32_t it0 = 0;          // ring position of the unit's K_0 (K_j at it0+2j, V_j at it0+2j+1)
+    uint32_t jt0 = 0, jt1 = 0;  // tiles each softmax group processed before this unit
+    int kx0 = 0, kx1 = 0;      // units each softmax group processed before this unit
+    uint32_t qu0 = 0, qu1 = 0;  // loads of each Q buffer consumed so far
     auto stage_of = [&](uint32_t pos) { return pos % C::kStages; };
     auto wait_full = [&](uint32_t pos, int site) -> bool {
         if (ptx::mbar_wait(sm.bar(C::BAR_FULL + stage_of(pos)), (pos / C::kStages) & 1u, lim, abort))
@@ -337,76 +411,130 @@ __device__ void mma_thread(const SplitParams& p, const Smem<NQ>& sm, uint32_t tm
         return false;
     };
     auto ring = [&](uint32_t pos) { return sm.base + C::kSmemRing + stage_of(pos) * kTileBytes; };
-    for (int ui = p.cta_first[blockIdx.x]; ui < p.cta_first[blockIdx.x + 1] && ok; ++ui) {
+    const int ui_end = p.cta_first[blockIdx.x + 1];
+    for (int ui = p.cta_first[blockIdx.x]; ui < ui_end && ok; ++ui) {
         const Unit u = p.units[ui];
         const int n = unit_tiles(u);
         if (n <= 0) continue;
-        const int nq = unit_nq<NQ>(u, p.tpt);
-        if (!ptx::mbar_wait(sm.bar(C::BAR_QFULL), k & 1, lim, abort)) { ok = false; record_timeout(p, abort, 10); break; }
+        const bool two = unit_nq<NQ>(u, p.tpt) == 2;
+        if (!ptx::mbar_wait(sm.bar(C::BAR_QFULL), qu0 & 1u, lim, abort) ||
+            (two && !ptx::mbar_wait(sm.bar(C::BAR_QFULL + 1), qu1 & 1u, lim, abort))) {
+            ok = false;
+            record_timeout(p, abort, 10);
+            break;
+        }
         for (int j = 0; j <= n && ok; ++j) {
-            const uint32_t posK = st.it0 + 2u * j, posV = posK + 1u, posVp = posK - 1u;
-            if (NQ == 2 && nq == 2) {
-                // S_0(j), P.V_1(j-1), S_1(j), P.V_0(j)
+            const uint32_t posK = it0 + 2u * j, posV = posK + 1u, posVp = posK - 1u;
+            if (two) {
                 if (j < n) {
                     if (!(ok = wait_full(posK, 11))) break;
-                    issue_s<NQ>(p, sm, tmem, st, 0, j, ring(posK));
+                    issue_s<NQ>(sm, tmem, 0, jt0 + j, ring(posK));
                     issued_any = true;
-                }
-                if (j > 0) {
-                    if (!(ok = issue_pv<NQ>(p, sm, tmem, st, 1, j - 1, ring(posVp)))) break;
-                    ptx::mma_commit(sm.bar(C::BAR_EMPTY + stage_of(posVp)));
-                }
-                if (j < n) {
-                    issue_s<NQ>(p, sm, tmem, st, 1, j, ring(posK));
-                    ptx::mma_commit(sm.bar(C::BAR_EMPTY + stage_of(posK)));
-                    if (j == n - 1) ptx::mma_commit(sm.bar(C::BAR_QFREE));
-                    if (!(ok = wait_full(posV, 13))) break;
-                    if (!(ok = issue_pv<NQ>(p, sm, tmem, st, 0, j, ring(posV)))) break;
-                }
-            } else if (NQ == 2) {
-                // one query tile only: S_0(j), P.V_0(j)
-                if (j < n) {
-                    if (!(ok = wait_full(posK, 11))) break;
-                    issue_s<NQ>(p, sm, tmem, st, 0, j, ring(posK));
-                    issued_any = true;
-                    ptx::mma_commit(sm.bar(C::BAR_EMPTY + stage_of(posK)));
-                    if (j == n - 1) ptx::mma_commit(sm.bar(C::BAR_QFREE));
-                    if (!(ok = wait_full(posV, 13))) break;
-                    if (!(ok = issue_pv<NQ>(p, sm, tmem, st, 0, j, ring(posV)))) break;
-                    ptx::mma_commit(sm.bar(C::BAR_EMPTY + stage_of(posV)));
-                }
-            } else {
-                // NQ == 1, S double-buffered: S(j), P.V(j-1). S(t) waits until the
-                // softmax has read S(t-1), so S-full never runs two phases ahead.
-                if (j < n) {
-                    if (!(ok = wait_full(posK, 11))) break;
-                    const uint32_t t = st.jt[0] + j;
-                    if (t > 0 && !ptx::mbar_wait(sm.gbar(0, SFREE), (t - 1) & 1u, lim, abort)) {
-                        ok = false;
-                        record_timeout(p, abort, 12);
-                        break;
-                    }
-                    issue_s<NQ>(p, sm, tmem, st, 0, j, ring(posK));
-                    issued_any = true;
-                    ptx::mma_commit(sm.bar(C::BAR_EMPTY + stage_of(posK)));
                     if (j == n - 1) ptx::mma_commit(sm.bar(C::BAR_QFREE));
                 }
                 if (j > 0) {
-                    if (!(ok = wait_full(posVp, 13))) break;
-                    if (!(ok = issue_pv<NQ>(p, sm, tmem, st, 0, j - 1, ring(posVp)))) break;
+                    const PvOp pv1{1, jt1 + j - 1, j == 1, kx1, posVp};
+                    if (!(ok = issue_pv<NQ>(p, sm, tmem, pv1, ring(posVp)))) break;
                     ptx::mma_commit(sm.bar(C::BAR_EMPTY + stage_of(posVp)));
                 }
+                if (j < n) {
+                    issue_s<NQ>(sm, tmem, 1, jt1 + j, ring(posK));
+                    ptx::mma_commit(sm.bar(C::BAR_EMPTY + stage_of(posK)));
+                    if (j == n - 1) ptx::mma_commit(sm.bar(C::BAR_QFREE + 1));
+                    if (!(ok = wait_full(posV, 13))) break;
+                    const PvOp pv0{0, jt0 + j, j == 0, kx0, posV};
+                    if (!(ok = issue_pv<NQ>(p, sm, tmem, pv0, ring(posV)))) break;
+                }
+            } else if (j < n) {
+                if (!(ok = wait_full(posK, 11))) break;
+                issue_s<NQ>(sm, tmem, 0, jt0 + j, ring(posK));
+                issued_any = true;
+                ptx::mma_commit(sm.bar(C::BAR_EMPTY + stage_of(posK)));
+                if (j == n - 1) ptx::mma_commit(sm.bar(C::BAR_QFREE));
+                if (!(ok = wait_full(posV, 13))) break;
+                const PvOp pv0{0, jt0 + j, j == 0, kx0, posV};
+                if (!(ok = issue_pv<NQ>(p, sm, tmem, pv0, ring(posV)))) break;
+                ptx::mma_commit(sm.bar(C::BAR_EMPTY + stage_of(posV)));
             }
         }
-        st.it0 += 2u * n;
-        st.jt[0] += n;
-        ++st.kx[0];
-        if (NQ == 2 && nq == 2) {  // static indices keep the counters in registers
-            st.jt[NQ - 1] += n;
-            ++st.kx[NQ - 1];
+        if (!ok) break;
+        it0 += 2u * n;
+        jt0 += n;
+        ++kx0;
+        ++qu0;
+        if (two) {
+            jt1 += n;
+            ++kx1;
+            ++qu1;
         }
-        ++k;
     }
+    if (!ok && issued_any) {
+        ptx::mma_commit(sm.bar(C::BAR_DRAIN));
+        ptx::mbar_wait(sm.bar(C::BAR_DRAIN), 0, lim, nullptr);
+    }
+}
+
+// The single tcgen05 issuer, one query tile per unit: S(t) into one of two S
+// buffers, then P.V(t-1), as one stream over all of the CTA's units (t counts
+// the CTA's tiles). A unit's last P.V is held back and issued after the next
+// unit's first S, so the S double buffer stays full across the boundary; if
+// that unit's Q has not landed yet the held P.V goes first.
+template <int NQ>
+__device__ void mma_thread_stream(const SplitParams& p, const Smem<NQ>& sm, uint32_t tmem) {
+    using C = Cfg<NQ>;
+    const uint64_t lim = p.wait_limit_ns;
+    volatile int* abort = sm.abort_flag();
+    bool ok = true;
+    bool issued_any = false;
+    uint32_t it0 = 0;   // ring position of the unit's K_0 (K_j at it0+2j, V_j at it0+2j+1)
+    uint32_t jt = 0;    // tiles processed before this unit
+    int kx = 0;         // units processed before this unit
+    uint32_t qu = 0;    // Q loads consumed so far
+    PvOp pend{0, 0, false, 0, 0};
+    bool has_pend = false;
+    const int ui_end = p.cta_first[blockIdx.x + 1];
+    for (int ui = p.cta_first[blockIdx.x]; ui < ui_end && ok; ++ui) {
+        const Unit u = p.units[ui];
+        const int n = unit_tiles(u);
+        if (n <= 0) continue;
+        if (has_pend && !ptx::mbar_test_wait(sm.bar(C::BAR_QFULL), qu & 1u) &&
+            !(ok = issue_held<NQ>(p, sm, tmem, pend, has_pend)))
+            break;
+        for (int j = 0; j < n && ok; ++j) {
+            const uint32_t posK = it0 + 2u * j, t = jt + j;
+            const uint32_t stage = posK % C::kStages;
+            if (!ptx::mbar_wait(sm.bar(C::BAR_FULL + stage), (posK / C::kStages) & 1u, lim, abort)) {
+                ok = false;
+                record_timeout(p, abort, 11);
+                break;
+            }
+            // S(t) waits until the softmax has read S(t-1), so S-full never runs
+            // two phases ahead
+            if (t > 0 && !ptx::mbar_wait(sm.gbar(0, SFREE), (t - 1) & 1u, lim, abort)) {
+                ok = false;
+                record_timeout(p, abort, 12);
+                break;
+            }
+            if (j == 0 && !ptx::mbar_wait(sm.bar(C::BAR_QFULL), qu & 1u, lim, abort)) {
+                ok = false;
+                record_timeout(p, abort, 10);
+                break;
+            }
+            issue_s<NQ>(sm, tmem, 0, t, sm.base + C::kSmemRing + stage * kTileBytes);
+            issued_any = true;
+            ptx::mma_commit(sm.bar(C::BAR_EMPTY + stage));
+            if (j == n - 1) ptx::mma_commit(sm.bar(C::BAR_QFREE));
+            if (!(ok = issue_held<NQ>(p, sm, tmem, pend, has_pend))) break;
+            pend = PvOp{0, t, j == 0, kx, posK + 1u};
+            has_pend = true;
+        }
+        if (!ok) break;
+        it0 += 2u * n;
+        jt += n;
+        ++kx;
+        ++qu;
+    }
+    if (ok) ok = issue_held<NQ>(p, sm, tmem, pend, has_pend);
     if (!ok && issued_any) {
         ptx::mma_commit(sm.bar(C::BAR_DRAIN));
         ptx::mbar_wait(sm.bar(C::BAR_DRAIN), 0, lim, nullptr);
@@ -587,18 +715,24 @@ __device__ void softmax_group(const SplitParams& p, const Smem<NQ>& sm, uint32_t
                                              __uint_as_float(r[8 * i + 5]) * inv_l),
                             ptx::pack_bf16x2(__uint_as_float(r[8 * i + 6]) * inv_l,
                                              __uint_as_float(r[8 * i + 7]) * inv_l));
-                } else {
-                    const float sc = direct ? inv_l : 1.f;
-                    float* base = direct ? static_cast<float*>(p.out) + orow * kHD
-                                         : p.part_o + (static_cast<int64_t>(ue.part) * rows_per_part +
-                                                       urow) * kHD;
-                    float4* dst = reinterpret_cast<float4*>(base + 32 * c);
+                } else if (direct) {
+                    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow * kHD +
+                                                            32 * c);
 #pragma unroll
                     for (int i = 0; i < 8; ++i)
-                        dst[i] = make_float4(__uint_as_float(r[4 * i + 0]) * sc,
-                                             __uint_as_float(r[4 * i + 1]) * sc,
-                                             __uint_as_float(r[4 * i + 2]) * sc,
-                                             __uint_as_float(r[4 * i + 3]) * sc);
+                        dst[i] = make_float4(__uint_as_float(r[4 * i + 0]) * inv_l,
+                                             __uint_as_float(r[4 * i + 1]) * inv_l,
+                                             __uint_as_float(r[4 * i + 2]) * inv_l,
+                                             __uint_as_float(r[4 * i + 3]) * inv_l);
+                } else {
+                    // Partial O (unnormalised): each thread writes its own row, so a
+                    // warp store touches 32 rows; 256-bit stores (whole sectors)
+                    // halve the store instructions. The partial buffer is 256-byte
+                    // aligned and rows are 512 bytes.
+                    float* dst = p.part_o +
+                                 (static_cast<int64_t>(ue.part) * rows_per_part + urow) * kHD + 32 * c;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) ptx::st_global_v8(dst + 8 * i, r + 8 * i);
                 }
             }
             if (row_valid) {
@@ -868,8 +1002,10 @@ __global__ void __launch_bounds__(Cfg<NQ>::kThreads, 1) __maxnreg__(NQ == 2 ? 20
             ptx::mbar_init(sm.bar(C::BAR_FULL + s), 1);
             ptx::mbar_init(sm.bar(C::BAR_EMPTY + s), 1);
         }
-        ptx::mbar_init(sm.bar(C::BAR_QFULL), 1);
-        ptx::mbar_init(sm.bar(C::BAR_QFREE), 1);
+        for (int x = 0; x < NQ; ++x) {
+            ptx::mbar_init(sm.bar(C::BAR_QFULL + x), 1);
+            ptx::mbar_init(sm.bar(C::BAR_QFREE + x), 1);
+        }
         ptx::mbar_init(sm.bar(C::BAR_AUX), 1);
         ptx::mbar_init(sm.bar(C::BAR_DRAIN), 1);
         for (int x = 0; x < NQ; ++x) {
@@ -902,7 +1038,10 @@ __global__ void __launch_bounds__(Cfg<NQ>::kThreads, 1) __maxnreg__(NQ == 2 ? 20
     if (warp == 0) {
         producer_warp<NQ>(p, sm, &tm_q, &tm_k, &tm_v);
     } else if (warp == 1) {
-        if (lane == 0) mma_thread<NQ>(p, sm, tmem);
+        if (lane == 0) {
+            if (NQ == 2) mma_thread_pair<NQ>(p, sm, tmem);
+            else mma_thread_stream<NQ>(p, sm, tmem);
+        }
         __syncwarp();
     } else {
         softmax_group<NQ>(p, sm, tmem, (warp - 2) >> 2);
