@@ -403,6 +403,7 @@ int fanout_lse_merge(const float* part_o, const float* part_ml, int32_t n_parts,
     m.part_o = part_o;
     m.part_ml = reinterpret_cast<const float2*>(part_ml);
     m.merge_cnt = nullptr;
+    m.merge_keys = nullptr;
     m.merge_ent = nullptr;
     m.merge_stride = 0;
     m.n_parts = n_parts;

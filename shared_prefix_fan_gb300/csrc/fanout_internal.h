@@ -43,6 +43,7 @@ struct PlanInput {
     int32_t causal;
     int32_t num_sms;       // persistent CTAs: at most one per SM
     int32_t force_splits;  // >0: cut every key range into this many chunks
+    int32_t tail_cuts = 1; // 0: never cut a direct range to even out the last wave
 };
 
 struct Plan {
@@ -50,6 +51,9 @@ struct Plan {
     std::vector<int32_t> cta_first;  // n_cta + 1 entries
     std::vector<int32_t> merge_cnt;  // R*H_kv: partial entries of (token, KV head)
     std::vector<int32_t> merge_ent;  // [R*H_kv][merge_stride] pairs {part, first row of the token}
+    // (token, KV head) keys that have partials, ascending; empty when every key
+    // has (then the merge visits every output row)
+    std::vector<int32_t> merge_keys;
     int32_t merge_stride = 0;
     int32_t n_parts = 0;             // partial blocks of 128 * nq rows
     int32_t R = 0;
@@ -67,9 +71,10 @@ struct MergeParams {
     const float2* part_ml;
     const int32_t* merge_cnt;  // null: uniform parts (n_parts per output, part-major)
     const int2* merge_ent;     // [key][stride] {part, row base}
+    const int32_t* merge_keys; // planned mode: keys to merge (null: every key)
     int32_t merge_stride;
     int32_t n_parts;           // uniform mode only
-    int64_t n_out;             // rows of out: R*H_q (or n for uniform mode)
+    int64_t n_out;             // rows to merge: R*H_q, |merge_keys|*G, or n (uniform mode)
     int32_t H_q, G;            // planned mode: out row n = token*H_q + kv_head*G + g
     int32_t rows_per_part;     // planned mode: rows of one partial block
     void* out;
@@ -127,7 +132,7 @@ struct CallArgs {
 
 // Device layout of a plan inside one scratch buffer.
 struct Layout {
-    size_t flags, units, cta, mcnt, ment, ml, o, total;
+    size_t flags, units, cta, mcnt, ment, mkeys, ml, o, total;
 };
 Layout plan_layout(const Plan& pl);
 // Copies the plan's tables into `base` (device) on `stream`.

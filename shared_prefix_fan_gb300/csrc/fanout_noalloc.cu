@@ -88,7 +88,13 @@ extern "C" FANOUT_API int fanout_attn_noalloc(
     PlanInput in{suffix_lens, q_rows_per_branch, num_branches, prefix_len, H_q, H_kv,
                  page_size, causal, sms > 0 ? sms : 1, current_force_splits()};
     if ((st = build_plan(in, plan)) != FANOUT_OK) return st;
-    const Layout L = plan_layout(plan);
+    Layout L = plan_layout(plan);
+    if (L.total > kScratchBytes) {
+        // without the tail cuts a long prefill has no partials at all
+        in.tail_cuts = 0;
+        if ((st = build_plan(in, plan)) != FANOUT_OK) return st;
+        L = plan_layout(plan);
+    }
     if (L.total > kScratchBytes) return FANOUT_ENOMEM;  // beyond the fixed array
 
     uint8_t* scratch = nullptr;

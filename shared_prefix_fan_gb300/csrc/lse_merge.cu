@@ -33,13 +33,13 @@ __global__ void __launch_bounds__(kMergeThreads, 1) lse_merge_kernel(const Merge
     const int lane = threadIdx.x & 31;
     const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
     const int64_t n0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    MergeIdx ix{0, 0, 0, make_int2(0, 0)};
+    MergeIdx ix{0, 0, 0, make_int2(0, 0), 0};
     if (n0 < p.n_out) {
         ix = merge_index(p, n0, lane);
-        merge_row_ix<kMergeBatch>(p, n0, ix, lane, true);
+        merge_row_ix<kMergeBatch>(p, ix, lane, true);
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (n0 < p.n_out) merge_row_ix<kMergeBatch>(p, n0, ix, lane);
+    if (n0 < p.n_out) merge_row_ix<kMergeBatch>(p, ix, lane);
     for (int64_t n = n0 + warps; n < p.n_out; n += warps) merge_row<kMergeBatch>(p, n, lane);
 }
 

@@ -21,32 +21,40 @@
 
 namespace fanout {
 
-// The merge index of one output row n (a (token, query head) pair): its
-// partial count ne, head-in-group g, and the first 32 entries. Planned mode:
-// fixed-stride entry lists {part, row base} per (token, KV head), partial row
-// = base + g. Uniform mode (merge_cnt null): n_parts partials per row,
-// part-major [n_parts][n_out]. Plan data only, so it may be read before the
-// partials exist.
+// The merge index of the i-th row to merge: its output row n (a (token, query
+// head) pair), partial count ne, head-in-group g, and the first 32 entries.
+// Planned mode: fixed-stride entry lists {part, row base} per (token, KV head),
+// partial row = base + g; the rows to merge are every output row, or the G
+// rows of each listed key when only some keys have partials. Uniform mode
+// (merge_cnt null): n_parts partials per row, part-major [n_parts][n_out].
+// Plan data only, so it may be read before the partials exist.
 struct MergeIdx {
     int32_t ne, g;
     int64_t key;
     int2 ent0;
+    int64_t n;
 };
-__device__ __forceinline__ MergeIdx merge_index(const MergeParams& p, int64_t n, int lane) {
-    MergeIdx ix{p.n_parts, 0, 0, make_int2(0, 0)};
+__device__ __forceinline__ MergeIdx merge_index(const MergeParams& p, int64_t i, int lane) {
+    MergeIdx ix{p.n_parts, 0, 0, make_int2(0, 0), i};
     if (p.merge_cnt != nullptr) {
         const int H_kv = p.H_q / p.G;
-        const int64_t tok = n / p.H_q;
-        const int32_t hq = static_cast<int32_t>(n % p.H_q);
-        ix.key = tok * H_kv + hq / p.G;
-        ix.g = hq % p.G;
+        if (p.merge_keys != nullptr) {
+            ix.key = __ldcg(p.merge_keys + i / p.G);
+            ix.g = static_cast<int32_t>(i % p.G);
+            ix.n = (ix.key / H_kv) * p.H_q + (ix.key % H_kv) * p.G + ix.g;
+        } else {
+            const int64_t tok = i / p.H_q;
+            const int32_t hq = static_cast<int32_t>(i % p.H_q);
+            ix.key = tok * H_kv + hq / p.G;
+            ix.g = hq % p.G;
+        }
         if (lane < p.merge_stride) ix.ent0 = __ldcg(p.merge_ent + ix.key * p.merge_stride + lane);
         ix.ne = __ldcg(p.merge_cnt + ix.key);
     }
     return ix;
 }
 
-// One warp merges output row n given its index. Up to kBatch partials per
+// One warp merges the row its index names (output row ix.n). Up to kBatch partials per
 // pass: lane e loads entry e's (m, l) while every lane loads its 4 columns of
 // all the pass's O vectors, in one memory round trip. Lanes past the count
 // load a valid duplicate row and get weight 0, so no load result is needed to
@@ -57,9 +65,10 @@ __device__ __forceinline__ MergeIdx merge_index(const MergeParams& p, int64_t n,
 // that cannot happen): run before the partials are final, it brings the code
 // and the merge index into the caches.
 template <int kBatch>
-__device__ __forceinline__ void merge_row_ix(const MergeParams& p, int64_t n,
-                                             const MergeIdx& ix, int lane, bool dry = false) {
+__device__ __forceinline__ void merge_row_ix(const MergeParams& p, const MergeIdx& ix, int lane,
+                                             bool dry = false) {
     const bool planned = p.merge_cnt != nullptr;
+    const int64_t n = ix.n;
     const int32_t ne = ix.ne;
     if (ne <= 0) return;  // written directly by the attention kernel
     float M = -INFINITY, L = 0.f;
@@ -131,8 +140,8 @@ __device__ __forceinline__ void merge_row_ix(const MergeParams& p, int64_t n,
 }
 
 template <int kBatch>
-__device__ __forceinline__ void merge_row(const MergeParams& p, int64_t n, int lane) {
-    merge_row_ix<kBatch>(p, n, merge_index(p, n, lane), lane);
+__device__ __forceinline__ void merge_row(const MergeParams& p, int64_t i, int lane) {
+    merge_row_ix<kBatch>(p, merge_index(p, i, lane), lane);
 }
 
 }  // namespace fanout

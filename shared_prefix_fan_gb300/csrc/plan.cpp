@@ -158,6 +158,89 @@ void make_streamk(const std::vector<Range>& ranges, int32_t max_cta, Cand& c) {
     c.cost = makespan + (n_parts > 0 ? kMergeLaunch + kMergePerPart * n_parts / c.n_cta : 0.0);
 }
 
+// Longest first with tail cuts: pieces go to the least-loaded CTA, largest
+// first (as in make_candidate with whole ranges); a piece that would lift that
+// CTA above the balanced load is cut there and its remainder goes back into
+// the queue. The leading waves keep the lockstep order of the whole-range plan
+// (the CTAs' first units read the same key chunks at about the same time) and
+// only the cut pieces become partials.
+void make_lpt_cut(const std::vector<Range>& ranges, int32_t max_cta, Cand& c) {
+    struct Piece {
+        int64_t work;
+        int32_t range;
+        int64_t t_lo;  // first tile of the piece within its range
+    };
+    int64_t total = 0;
+    std::vector<int64_t> nkt(ranges.size());
+    for (size_t i = 0; i < ranges.size(); ++i) {
+        nkt[i] = cdiv(ranges[i].hi - ranges[i].lo, kBN);
+        total += nkt[i];
+    }
+    const int32_t n_cta = static_cast<int32_t>(std::min<int64_t>(max_cta, total));
+    const double target = (static_cast<double>(total) +
+                           kUnitOverhead * static_cast<double>(ranges.size() + n_cta)) / n_cta;
+    auto key = [&](const Piece& a) {
+        const Range& r = ranges[a.range];
+        return std::make_tuple(-a.work, r.lo + static_cast<int32_t>(a.t_lo) * kBN, r.kv_head,
+                               r.branch, r.tok_begin);
+    };
+    auto later = [&](const Piece& a, const Piece& b) { return key(b) < key(a); };
+    std::priority_queue<Piece, std::vector<Piece>, decltype(later)> queue(later);
+    for (size_t i = 0; i < ranges.size(); ++i)
+        if (nkt[i] > 0) queue.push(Piece{nkt[i], static_cast<int32_t>(i), 0});
+    using Slot = std::pair<double, int32_t>;
+    std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
+    for (int32_t i = 0; i < n_cta; ++i) heap.push({0.0, i});
+    c.units.clear();
+    c.work.clear();
+    c.cta_of.clear();
+    std::vector<bool> cut(ranges.size(), false);
+    std::vector<int32_t> range_of;
+    double makespan = 0;
+    while (!queue.empty()) {
+        Piece pc = queue.top();
+        queue.pop();
+        Slot s = heap.top();
+        heap.pop();
+        int64_t take = pc.work;
+        const double room = target - s.first - kUnitOverhead;
+        if (s.first + kUnitOverhead + static_cast<double>(pc.work) > target + 0.5 && room >= 1.0 &&
+            pc.work >= 2) {
+            take = std::min<int64_t>(pc.work - 1, static_cast<int64_t>(room));
+            queue.push(Piece{pc.work - take, pc.range, pc.t_lo + take});
+            cut[pc.range] = true;
+        }
+        const Range& r = ranges[pc.range];
+        const int32_t k_lo = r.lo + static_cast<int32_t>(pc.t_lo) * kBN;
+        const int32_t k_hi = std::min<int32_t>(r.hi, r.lo + static_cast<int32_t>(pc.t_lo + take) * kBN);
+        c.units.push_back(Unit{r.kv_head, r.branch, r.tok_begin, r.n_tok, k_lo, k_hi, r.pos_base, 0});
+        c.work.push_back(take);
+        c.cta_of.push_back(s.second);
+        range_of.push_back(pc.range);
+        s.first += static_cast<double>(take) + kUnitOverhead;
+        makespan = std::max(makespan, s.first);
+        heap.push(s);
+    }
+    // CTAs that received nothing (fewer pieces than CTAs) are dropped
+    std::vector<int32_t> renum(n_cta, -1);
+    int32_t used = 0;
+    for (int32_t& cta : c.cta_of) {
+        if (renum[cta] < 0) renum[cta] = used++;
+        cta = renum[cta];
+    }
+    // a range left whole that covers every visible key of its rows is written
+    // directly; every other piece is a partial
+    int64_t n_parts = 0;
+    for (size_t i = 0; i < c.units.size(); ++i) {
+        const int32_t ri = range_of[i];
+        const bool whole = ranges[ri].complete && !cut[ri];
+        c.units[i].part = whole ? -1 : 0;
+        if (!whole) ++n_parts;
+    }
+    c.n_cta = used;
+    c.cost = makespan + (n_parts > 0 ? kMergeLaunch + kMergePerPart * n_parts / c.n_cta : 0.0);
+}
+
 }  // namespace
 
 int build_plan(const PlanInput& in, Plan& plan) {
@@ -239,6 +322,16 @@ int build_plan(const PlanInput& in, Plan& plan) {
                 first = false;
             }
         }
+        // Tail cuts when every range is written directly (long prefill): the
+        // cut pieces are then the only partials. With split ranges the
+        // equal-chunk plans above already balance, and measured faster: the
+        // cuts' remainders pile onto the CTAs that hold many short units.
+        bool all_complete = true;
+        for (const Range& r : ranges) all_complete = all_complete && r.complete;
+        if (all_complete && in.tail_cuts) {
+            make_lpt_cut(ranges, max_cta, cand);
+            if (cand.cost < best.cost * 0.995) std::swap(best, cand);
+        }
         // Exact balance scatters CTAs over different key offsets; use it only
         // when the whole KV fits in L2 (otherwise the lockstep waves of the
         // equal-chunk plan are what keeps a large shared prefix in L2).
@@ -288,7 +381,13 @@ int build_plan(const PlanInput& in, Plan& plan) {
                     plan.merge_ent[2 * e] = u.part;
                     plan.merge_ent[2 * e + 1] = (t - u.tok_begin) * G;  // first row of t in u
                 }
-        // a (token, head) covered by a single direct unit has count 0
+        // a (token, head) covered by a single direct unit has count 0; when
+        // some are, the merge visits only the keys listed here
+        bool sparse = false;
+        for (int32_t c : plan.merge_cnt) sparse = sparse || c == 0;
+        if (sparse)
+            for (size_t k = 0; k < n_keys; ++k)
+                if (plan.merge_cnt[k] > 0) plan.merge_keys.push_back(static_cast<int32_t>(k));
     }
     plan.need_merge = n_parts > 0;
     return 0;

@@ -121,6 +121,8 @@ Layout plan_layout(const Plan& pl) {
     off = align256(off + pl.merge_cnt.size() * sizeof(int32_t));
     L.ment = off;
     off = align256(off + pl.merge_ent.size() * sizeof(int32_t));
+    L.mkeys = off;
+    off = align256(off + pl.merge_keys.size() * sizeof(int32_t));
     L.ml = off;
     const size_t rows = static_cast<size_t>(pl.n_parts) * kBM * pl.nq;
     off = align256(off + rows * sizeof(float2));
@@ -142,6 +144,9 @@ cudaError_t upload_plan(const Plan& pl, const Layout& L, uint8_t* base, cudaStre
     if (e == cudaSuccess && !pl.merge_ent.empty())
         e = cudaMemcpyAsync(base + L.ment, pl.merge_ent.data(),
                             pl.merge_ent.size() * sizeof(int32_t), cudaMemcpyHostToDevice, stream);
+    if (e == cudaSuccess && !pl.merge_keys.empty())
+        e = cudaMemcpyAsync(base + L.mkeys, pl.merge_keys.data(),
+                            pl.merge_keys.size() * sizeof(int32_t), cudaMemcpyHostToDevice, stream);
     return e;
 }
 
@@ -185,9 +190,10 @@ int launch_plan(const CallArgs& a, const Plan& pl, const Layout& L, uint8_t* bas
     m.part_ml = p.part_ml;
     m.merge_cnt = reinterpret_cast<const int32_t*>(base + L.mcnt);
     m.merge_ent = reinterpret_cast<const int2*>(base + L.ment);
+    m.merge_keys = pl.merge_keys.empty() ? nullptr : reinterpret_cast<const int32_t*>(base + L.mkeys);
     m.merge_stride = pl.merge_stride;
     m.n_parts = 0;
-    m.n_out = a.R * a.H_q;
+    m.n_out = pl.merge_keys.empty() ? a.R * a.H_q : static_cast<int64_t>(pl.merge_keys.size()) * G;
     m.H_q = a.H_q;
     m.G = G;
     m.rows_per_part = kBM * pl.nq;
@@ -197,13 +203,13 @@ int launch_plan(const CallArgs& a, const Plan& pl, const Layout& L, uint8_t* bas
     p.flags = reinterpret_cast<uint32_t*>(base + L.flags);
     p.epoch = a.epoch;
     // The merge runs inside the attention kernel when every CTA can be resident
-    // at once (one per SM); otherwise, or if the cooperative launch is refused,
-    // as a separate kernel.
+    // at once (one per SM) and every output row has partials; otherwise, or if
+    // the cooperative launch is refused, as a separate kernel.
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const bool fuse = pl.need_merge && a.fused_merge && pl.n_cta() <= kMaxFusedGrid &&
-                      pl.n_cta() <= sms;
+    const bool fuse = pl.need_merge && a.fused_merge && pl.merge_keys.empty() &&
+                      pl.n_cta() <= kMaxFusedGrid && pl.n_cta() <= sms;
 
     if (ev_before) cudaEventRecord(ev_before, stream);
     p.fused_merge = fuse ? 1 : 0;

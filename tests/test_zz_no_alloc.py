@@ -55,3 +55,17 @@ def test_noalloc_rejects_problem_beyond_scratch():
         binding.set_option(binding.OPT_SPLITS, 0)
     torch.cuda.synchronize()
     assert (out == 0).all().item()   # nothing ran
+
+
+def test_noalloc_long_prefill():
+    """A long prefill: fanout_attn cuts a few query blocks to even out the last
+    wave (their partials are merged); the fixed scratch array cannot hold those
+    partials, so the no-allocation entry plans without the cuts. Both give the
+    same attention."""
+    dw = DevWorkload(draw(WORKLOADS["prefill"]))
+    ref_out, ref_lse = dw.run()
+    out = torch.full_like(ref_out, float("nan"))
+    lse = torch.full_like(ref_lse, float("nan"))
+    assert _noalloc(dw, out, lse) == binding.OK
+    assert binding.last_error() == binding.OK
+    _close(out, lse, ref_out, ref_lse)
