@@ -76,7 +76,11 @@ struct Cfg {
     static constexpr int BAR_GROUP = BAR_DRAIN + 1;  // + 5 x + {SFULL, PFULL, ODONE, OFREE, SFREE}
     static constexpr int kNumBars = BAR_GROUP + 5 * NQ;
     static constexpr int kSmemMisc = kSmemBar + kNumBars * 8;
-    static constexpr int kSmemTotal = kSmemMisc + 16;
+    // 16 bytes per warp (16-byte aligned for the vector accesses): the output
+    // fields of a softmax warp's current unit
+    static constexpr int kSmemWarp = (kSmemMisc + 16 + 15) & ~15;
+    static constexpr int kSmemTotal = kSmemWarp + 16 * (kThreads / 32);
+    static_assert(kSmemWarp % 16 == 0 && kSmemBar % 1024 == 0, "shared-memory alignment");
     static constexpr int kSmemAlloc = kSmemTotal + 1024;  // base aligned up to 1024 B
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kColO = 256;
@@ -117,12 +121,6 @@ __device__ __forceinline__ void record_timeout(const SplitParams& p, volatile in
         p.err[1] = site;
         p.err[2] = static_cast<int32_t>(blockIdx.x);
     }
-}
-
-// A unit re-read from memory (volatile: not kept in registers from an earlier read).
-__device__ __forceinline__ Unit load_unit_volatile(const Unit* up) {
-    const volatile int32_t* v = reinterpret_cast<const volatile int32_t*>(up);
-    return Unit{v[0], v[1], v[2], v[3], v[4], v[5], v[6], v[7]};
 }
 
 __device__ __forceinline__ int unit_tiles(const Unit& u) {
@@ -566,17 +564,33 @@ __device__ void softmax_group(const SplitParams& p, const Smem<NQ>& sm, uint32_t
     volatile int* abort = sm.abort_flag();
     const float sl2 = p.scale_log2;
     const int rows_per_part = kBM * NQ;
+    // the epilogue's fields of the current unit (token start, KV head, partial
+    // block), kept in this warp's shared-memory slot rather than in registers
+    // through the tile loop or re-read from global memory under load
+    const uint32_t slot = sm.base + C::kSmemWarp + 16u * warp;
     uint32_t jt = 0;
     bool ok = true;
-    for (int ui = p.cta_first[blockIdx.x]; ui < p.cta_first[blockIdx.x + 1] && ok; ++ui) {
-        const Unit u = p.units[ui];
-        const int n_tiles = unit_tiles(u);
-        if (n_tiles <= 0 || x >= unit_nq<NQ>(u, p.tpt)) continue;
+    // Before the first unit the group makes a dry run of the epilogue (no
+    // tiles, no waits, one thread's stores into a scratch sink) while it waits
+    // for its first K/V tile anyway: the epilogue code is otherwise first
+    // fetched in the middle of the kernel, from a cold instruction cache, with
+    // the memory system saturated by the other CTAs (measured: a unit's first
+    // epilogue took 6-7 us in decode, a later one 0.8 us).
+    const int ui_first = p.cta_first[blockIdx.x], ui_end = p.cta_first[blockIdx.x + 1];
+    for (int ui = ui_first < ui_end ? ui_first - 1 : ui_first; ui < ui_end && ok; ++ui) {
+        const bool dry = ui < ui_first;
+        const Unit u = p.units[dry ? ui_first : ui];
+        const int n_tiles = dry ? 0 : unit_tiles(u);
+        if (!dry && (n_tiles <= 0 || x >= unit_nq<NQ>(u, p.tpt))) continue;
         const int urow = kBM * x + row;  // row within the unit
-        const bool row_valid = urow < u.n_tok * p.G;
-        const bool active = __any_sync(0xffffffffu, row_valid);
+        const bool row_valid = dry ? (lane == 0 && quarter == 0) : urow < u.n_tok * p.G;
+        if (lane == 0)
+            ptx::st_shared_v4(slot, static_cast<uint32_t>(u.tok_begin), static_cast<uint32_t>(u.kv_head),
+                              static_cast<uint32_t>(u.part), 0u);
+        __syncwarp();
+        const bool active = dry || __any_sync(0xffffffffu, row_valid);
         // Only the key start and this row's visible end stay live through the
-        // tile loop (registers); the epilogue reads the unit again.
+        // tile loop (registers).
         const int key_begin = u.key_begin;
         const int vis_end = row_valid ? min(u.key_end, u.pos_base + u.tok_begin + urow / p.G + 1) : 0;
         float m_ref = -INFINITY, l_run = 0.f;
@@ -683,16 +697,26 @@ __device__ void softmax_group(const SplitParams& p, const Smem<NQ>& sm, uint32_t
             if (lane == 0) ptx::mbar_arrive(sm.gbar(x, PFULL));
         }
         if (!ok) break;
-        // Epilogue: the last P.V done -> this row of O to global memory.
-        bool w = ptx::mbar_wait(sm.gbar(x, ODONE), (jt - 1) & 1u, lim, abort);
-        if (!__all_sync(0xffffffffu, w)) { ok = false; record_timeout(p, abort, 22); break; }
+        // Epilogue: the last P.V done -> this row of O to global memory (the
+        // dry run: O's TMEM columns are not written before the first P.V, which
+        // waits for this group; its stores go to the sink).
+        if (!dry) {
+            bool w = ptx::mbar_wait(sm.gbar(x, ODONE), (jt - 1) & 1u, lim, abort);
+            if (!__all_sync(0xffffffffu, w)) { ok = false; record_timeout(p, abort, 22); break; }
+        }
         ptx::tc_fence_after();
         if (active) {
-            const Unit ue = load_unit_volatile(p.units + ui);
-            const int tok = ue.tok_begin + urow / p.G;
-            const int hq = ue.kv_head * p.G + urow % p.G;
-            const int64_t orow = static_cast<int64_t>(tok) * p.H_q + hq;
-            const bool direct = ue.part < 0;
+            const uint4 f = ptx::ld_shared_v4(slot);
+            const int e_part = static_cast<int>(f.z);
+            const int tok = static_cast<int>(f.x) + urow / p.G;
+            const int hq = static_cast<int>(f.y) * p.G + urow % p.G;
+            const int64_t orow = dry ? 0 : static_cast<int64_t>(tok) * p.H_q + hq;
+            const int64_t prow = dry ? 0 : static_cast<int64_t>(e_part) * rows_per_part + urow;
+            void* const out_base = dry ? static_cast<void*>(p.sink) : p.out;
+            float* const po_base = dry ? p.sink : p.part_o;
+            float* const lse_base = dry ? p.sink : p.lse;
+            float2* const ml_base = dry ? reinterpret_cast<float2*>(p.sink) : p.part_ml;
+            const bool direct = e_part < 0;
             const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
@@ -702,7 +726,7 @@ __device__ void softmax_group(const SplitParams& p, const Smem<NQ>& sm, uint32_t
                 ptx::tmem_ld_wait(r);
                 if (!row_valid) {
                 } else if (direct && p.out_bf16) {
-                    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) +
+                    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out_base) +
                                                           orow * kHD + 32 * c);
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
@@ -716,8 +740,8 @@ __device__ void softmax_group(const SplitParams& p, const Smem<NQ>& sm, uint32_t
                             ptx::pack_bf16x2(__uint_as_float(r[8 * i + 6]) * inv_l,
                                              __uint_as_float(r[8 * i + 7]) * inv_l));
                 } else if (direct) {
-                    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow * kHD +
-                                                            32 * c);
+                    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out_base) +
+                                                            orow * kHD + 32 * c);
 #pragma unroll
                     for (int i = 0; i < 8; ++i)
                         dst[i] = make_float4(__uint_as_float(r[4 * i + 0]) * inv_l,
@@ -729,24 +753,22 @@ __device__ void softmax_group(const SplitParams& p, const Smem<NQ>& sm, uint32_t
                     // warp store touches 32 rows; 256-bit stores (whole sectors)
                     // halve the store instructions. The partial buffer is 256-byte
                     // aligned and rows are 512 bytes.
-                    float* dst = p.part_o +
-                                 (static_cast<int64_t>(ue.part) * rows_per_part + urow) * kHD + 32 * c;
+                    float* dst = po_base + prow * kHD + 32 * c;
 #pragma unroll
                     for (int i = 0; i < 4; ++i) ptx::st_global_v8(dst + 8 * i, r + 8 * i);
                 }
             }
             if (row_valid) {
                 if (direct) {
-                    if (p.lse) p.lse[orow] = (m_ref + __log2f(l_run)) * 0.69314718055994531f;
+                    if (lse_base) lse_base[orow] = (m_ref + __log2f(l_run)) * 0.69314718055994531f;
                 } else {
-                    p.part_ml[static_cast<int64_t>(ue.part) * rows_per_part + urow] =
-                        make_float2(m_ref, l_run);
+                    ml_base[prow] = make_float2(m_ref, l_run);
                 }
             }
         }
         ptx::tc_fence_before();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(sm.gbar(x, OFREE));
+        if (lane == 0 && !dry) ptx::mbar_arrive(sm.gbar(x, OFREE));
     }
 }
 

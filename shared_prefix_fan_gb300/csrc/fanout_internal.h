@@ -92,6 +92,7 @@ struct SplitParams {
     const Unit* units;
     const int32_t* cta_first;
     float* part_o;    // [part][128 * nq rows][kHD]
+    float* sink;      // kSinkBytes of scratch: the epilogue's dry-run stores
     float2* part_ml;  // [part][128 * nq rows]   (m in log2 units, l)
     void* out;        // [R][H_q][kHD] fp32 or bf16
     float* lse;       // [R][H_q] or null
@@ -131,8 +132,12 @@ struct CallArgs {
 };
 
 // Device layout of a plan inside one scratch buffer.
+// Scratch the attention kernel's dry-run epilogue stores into (one row of O
+// and its (m, l); written by every CTA, never read).
+constexpr size_t kSinkBytes = 1024;
+
 struct Layout {
-    size_t flags, units, cta, mcnt, ment, mkeys, ml, o, total;
+    size_t flags, sink, units, cta, mcnt, ment, mkeys, ml, o, total;
 };
 Layout plan_layout(const Plan& pl);
 // Copies the plan's tables into `base` (device) on `stream`.

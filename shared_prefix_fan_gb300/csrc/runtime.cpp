@@ -113,6 +113,8 @@ Layout plan_layout(const Plan& pl) {
     size_t off = 0;
     L.flags = off;  // always first: epochs of the fused merge (zero when first allocated)
     off = align256(off + kMaxFusedGrid * sizeof(uint32_t));
+    L.sink = off;
+    off = align256(off + kSinkBytes);
     L.units = off;
     off = align256(off + pl.units.size() * sizeof(Unit));
     L.cta = off;
@@ -170,6 +172,7 @@ int launch_plan(const CallArgs& a, const Plan& pl, const Layout& L, uint8_t* bas
     p.cta_first = reinterpret_cast<const int32_t*>(base + L.cta);
     p.part_o = reinterpret_cast<float*>(base + L.o);
     p.part_ml = reinterpret_cast<float2*>(base + L.ml);
+    p.sink = reinterpret_cast<float*>(base + L.sink);
     p.out = a.out;
     p.lse = a.lse;
     p.err = err;
