@@ -47,7 +47,11 @@ struct Range {
 
 inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-constexpr double kUnitOverhead = 2.0;  // prologue + epilogue of a unit, in tile times
+// Prologue + epilogue of a unit, in tile times: two query tiles per unit
+// (tensor-bound tiles of ~1.8 us) and one (HBM-bound tiles of ~1.4 us, whose
+// unit boundaries measured 3-5 us).
+constexpr double kUnitOverhead2 = 2.0;
+constexpr double kUnitOverhead1 = 3.0;
 constexpr double kMergePerPart = 2.0;  // write + read of one 128-row partial, in tile times
 constexpr double kMergeLaunch = 4.0;   // the extra merge launch, in tile times
 
@@ -61,7 +65,7 @@ struct Cand {
 
 // Cut the ranges with chunk size `chunk` tiles (0 = whole ranges), sort, assign.
 void make_candidate(const std::vector<Range>& ranges, int64_t chunk, int32_t force_splits,
-                    int32_t max_cta, Cand& c) {
+                    int32_t max_cta, double unit_ovh, Cand& c) {
     struct Keyed {
         int64_t work;
         Unit u;
@@ -98,7 +102,7 @@ void make_candidate(const std::vector<Range>& ranges, int64_t chunk, int32_t for
     for (const Keyed& k : all) {
         Slot s = heap.top();
         heap.pop();
-        s.first += static_cast<double>(k.work) + kUnitOverhead;
+        s.first += static_cast<double>(k.work) + unit_ovh;
         makespan = std::max(makespan, s.first);
         heap.push(s);
         Unit u = k.u;
@@ -114,14 +118,14 @@ void make_candidate(const std::vector<Range>& ranges, int64_t chunk, int32_t for
 // Exact-balance candidate (Stream-K style): the ranges' tiles laid end to end
 // and cut into one contiguous quota per CTA; a CTA's quota may end inside a
 // range and the next CTA continues it.
-void make_streamk(const std::vector<Range>& ranges, int32_t max_cta, Cand& c) {
+void make_streamk(const std::vector<Range>& ranges, int32_t max_cta, double unit_ovh, Cand& c) {
     int64_t total = 0;
     for (const Range& r : ranges) total += cdiv(r.hi - r.lo, kBN);
     const int32_t n_cta = static_cast<int32_t>(std::min<int64_t>(max_cta, total));
     // per-CTA quota in tile times, counting one unit overhead per range and per
     // cut (about one cut per CTA)
     const double quota = (static_cast<double>(total) +
-                          kUnitOverhead * static_cast<double>(ranges.size() + n_cta)) / n_cta;
+                          unit_ovh * static_cast<double>(ranges.size() + n_cta)) / n_cta;
     c.units.clear();
     c.work.clear();
     c.cta_of.clear();
@@ -132,7 +136,7 @@ void make_streamk(const std::vector<Range>& ranges, int32_t max_cta, Cand& c) {
         const int64_t nkt = cdiv(r.hi - r.lo, kBN);
         int64_t t = 0;
         while (t < nkt) {
-            const double room = quota - load[cta] - kUnitOverhead;
+            const double room = quota - load[cta] - unit_ovh;
             if (room < 0.5 && load[cta] > 0 && cta + 1 < n_cta) {
                 ++cta;
                 continue;
@@ -148,7 +152,7 @@ void make_streamk(const std::vector<Range>& ranges, int32_t max_cta, Cand& c) {
             if (!whole) ++n_parts;
             c.work.push_back(take);
             c.cta_of.push_back(cta);
-            load[cta] += static_cast<double>(take) + kUnitOverhead;
+            load[cta] += static_cast<double>(take) + unit_ovh;
             t += take;
         }
     }
@@ -164,7 +168,7 @@ void make_streamk(const std::vector<Range>& ranges, int32_t max_cta, Cand& c) {
 // the queue. The leading waves keep the lockstep order of the whole-range plan
 // (the CTAs' first units read the same key chunks at about the same time) and
 // only the cut pieces become partials.
-void make_lpt_cut(const std::vector<Range>& ranges, int32_t max_cta, Cand& c) {
+void make_lpt_cut(const std::vector<Range>& ranges, int32_t max_cta, double unit_ovh, Cand& c) {
     struct Piece {
         int64_t work;
         int32_t range;
@@ -178,7 +182,7 @@ void make_lpt_cut(const std::vector<Range>& ranges, int32_t max_cta, Cand& c) {
     }
     const int32_t n_cta = static_cast<int32_t>(std::min<int64_t>(max_cta, total));
     const double target = (static_cast<double>(total) +
-                           kUnitOverhead * static_cast<double>(ranges.size() + n_cta)) / n_cta;
+                           unit_ovh * static_cast<double>(ranges.size() + n_cta)) / n_cta;
     auto key = [&](const Piece& a) {
         const Range& r = ranges[a.range];
         return std::make_tuple(-a.work, r.lo + static_cast<int32_t>(a.t_lo) * kBN, r.kv_head,
@@ -203,8 +207,8 @@ void make_lpt_cut(const std::vector<Range>& ranges, int32_t max_cta, Cand& c) {
         Slot s = heap.top();
         heap.pop();
         int64_t take = pc.work;
-        const double room = target - s.first - kUnitOverhead;
-        if (s.first + kUnitOverhead + static_cast<double>(pc.work) > target + 0.5 && room >= 1.0 &&
+        const double room = target - s.first - unit_ovh;
+        if (s.first + unit_ovh + static_cast<double>(pc.work) > target + 0.5 && room >= 1.0 &&
             pc.work >= 2) {
             take = std::min<int64_t>(pc.work - 1, static_cast<int64_t>(room));
             queue.push(Piece{pc.work - take, pc.range, pc.t_lo + take});
@@ -217,7 +221,7 @@ void make_lpt_cut(const std::vector<Range>& ranges, int32_t max_cta, Cand& c) {
         c.work.push_back(take);
         c.cta_of.push_back(s.second);
         range_of.push_back(pc.range);
-        s.first += static_cast<double>(take) + kUnitOverhead;
+        s.first += static_cast<double>(take) + unit_ovh;
         makespan = std::max(makespan, s.first);
         heap.push(s);
     }
@@ -298,9 +302,10 @@ int build_plan(const PlanInput& in, Plan& plan) {
 
     // Chunk size from the cost model (or the forced split count).
     const int32_t max_cta = std::max(1, in.num_sms);
+    const double ovh = plan.nq == 2 ? kUnitOverhead2 : kUnitOverhead1;
     Cand best, cand;
     if (in.force_splits > 0) {
-        make_candidate(ranges, 0, in.force_splits, max_cta, best);
+        make_candidate(ranges, 0, in.force_splits, max_cta, ovh, best);
     } else {
         int64_t max_nkt = 1;
         for (const Range& r : ranges) max_nkt = std::max(max_nkt, cdiv(r.hi - r.lo, kBN));
@@ -309,14 +314,15 @@ int build_plan(const PlanInput& in, Plan& plan) {
             std::max<int64_t>(16LL * max_cta, static_cast<int64_t>(ranges.size()));
         bool first = true;
         for (int64_t chunk : {0LL, 1024LL, 512LL, 384LL, 256LL, 192LL, 128LL, 96LL, 64LL, 48LL,
-                              32LL, 24LL, 16LL, 12LL, 8LL, 6LL, 4LL, 3LL, 2LL}) {
+                              40LL, 32LL, 28LL, 24LL, 20LL, 18LL, 16LL, 14LL, 12LL, 10LL, 8LL, 6LL,
+                              4LL, 3LL, 2LL}) {
             if (chunk > 0 && chunk >= max_nkt) continue;  // same as whole ranges
             if (chunk > 0) {
                 int64_t n = 0;
                 for (const Range& r : ranges) n += cdiv(cdiv(r.hi - r.lo, kBN), chunk);
                 if (n > max_units) continue;
             }
-            make_candidate(ranges, chunk, 0, max_cta, cand);
+            make_candidate(ranges, chunk, 0, max_cta, ovh, cand);
             if (first || cand.cost < best.cost * 0.995) {
                 std::swap(best, cand);
                 first = false;
@@ -329,7 +335,7 @@ int build_plan(const PlanInput& in, Plan& plan) {
         bool all_complete = true;
         for (const Range& r : ranges) all_complete = all_complete && r.complete;
         if (all_complete && in.tail_cuts) {
-            make_lpt_cut(ranges, max_cta, cand);
+            make_lpt_cut(ranges, max_cta, ovh, cand);
             if (cand.cost < best.cost * 0.995) std::swap(best, cand);
         }
         // Exact balance scatters CTAs over different key offsets; use it only
@@ -339,7 +345,7 @@ int build_plan(const PlanInput& in, Plan& plan) {
         for (int32_t b = 0; b < B; ++b) kv_tokens += S_eff[b];
         const int64_t kv_bytes = kv_tokens * in.H_kv * kHD * 2 * 2;
         if (kv_bytes <= (100LL << 20)) {
-            make_streamk(ranges, max_cta, cand);
+            make_streamk(ranges, max_cta, ovh, cand);
             if (cand.cost < best.cost * 0.97) std::swap(best, cand);
         }
     }
