@@ -37,9 +37,15 @@
 // Issue order of the MMA thread per K/V tile j:
 //   NQ = 2: S_0(j), P.V_1(j-1), S_1(j), P.V_0(j): while one softmax group
 //           works, the tensor core runs the other group's products;
-//   NQ = 1: S(j), P.V(j-1): S of the next tile overlaps the softmax.
+//   NQ = 1: S(j), P.V(j-1): S of the next tile overlaps the softmax; this
+//           runs as one stream over all of the CTA's units.
 // Since tcgen05 operations of one thread execute in order, an S that reuses
 // the TMEM holding an earlier P is issued after the P.V that reads that P.
+// Unit boundaries: the producer issues the next unit's first K/V tile before
+// it waits for the Q buffer (one Q full/free barrier pair per query tile) and
+// brings the next unit's Q into L2 one unit ahead; each softmax warp keeps its
+// unit's output fields in a shared-memory slot, and each group runs its
+// epilogue once dry before the first unit so that code is warm.
 // Every wait is bounded (mbar_wait); on expiry the CTA records
 // FANOUT_ETIMEOUT, drains its own in-flight copies and MMAs, frees TMEM and
 // returns.
