@@ -18,6 +18,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import subprocess
@@ -76,10 +77,19 @@ def load_peaks():
     return dict(hbm=6800.0, tc=1900.0, tc_sustained=1700.0, source="fallback")
 
 
+def source_code_text(text: str) -> str:
+    """C++ source with comments removed and whitespace collapsed: what the
+    compiler sees, so an edit to a comment does not retire a measurement."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_sha() -> str:
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        h.update(open(os.path.join(ROOT, "shared_prefix_fan_gb300", "csrc", f), "rb").read())
+        with open(os.path.join(ROOT, "shared_prefix_fan_gb300", "csrc", f)) as fh:
+            h.update(source_code_text(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

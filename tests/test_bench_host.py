@@ -27,3 +27,14 @@ def test_decode_bytes():
     work = bench.algorithmic_work(w)
     assert work["kv_bytes"] == (32768 + 8 * 512) * 8 * 128 * 2 * 2
     assert work["flops"] == 4 * 128 * 64 * 8 * (32768 + 512)
+
+
+def test_kernel_fingerprint_ignores_comments_only():
+    """The ncu traffic stays attached to a kernel whose comments changed, and
+    is dropped as soon as its code changes."""
+    code = "int f(int a) {\n  return a + 1;  // add one\n}\n/* block\n comment */\n"
+    assert bench.source_code_text(code) == bench.source_code_text(
+        "int f(int a) { return a + 1; }  // other words\n")
+    assert bench.source_code_text(code) != bench.source_code_text("int f(int a) { return a + 2; }")
+    assert bench.source_code_text('asm("ld.global.v4.s32 {%0}, [%1];");') == \
+        'asm("ld.global.v4.s32 {%0}, [%1];");'
