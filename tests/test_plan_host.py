@@ -134,3 +134,14 @@ def test_plan_random(seed):
         check_plan(S, T, P, hq, hkv, ps, causal, sms)
     finally:
         binding.set_option(binding.OPT_SPLITS, 0)
+
+
+def test_plan_decode_unit_counts():
+    """Decode (one query tile per unit): a unit boundary costs about three
+    HBM-bound tile times, so no CTA is given more than two units (measured:
+    CTAs with three 4-tile suffix units finished last)."""
+    w = draw(WORKLOADS["decode"])
+    s = w.spec
+    units, cta, _ = check_plan(w.suffix_lens, w.q_rows, s.prefix_len, s.h_q, s.h_kv,
+                               s.page_size, s.causal, sms=152)
+    assert np.diff(cta).max() <= 2
