@@ -281,6 +281,21 @@ FANOUT_API int fanout_plan(const int32_t *suffix_lens, const int32_t *q_rows_per
                 int32_t cap, int32_t *n_units, int32_t *cta_first, int32_t cta_cap,
                 int32_t *n_ctas, int32_t *n_parts);
 
+/* The plan fanout_attn runs for a call whose previous call on the same stream
+ * had the same arguments except the suffix lengths, prev_suffix_lens (a decode
+ * step: each branch's suffix grew by the tokens just appended). When every key
+ * range keeps its number of 128-key tiles, the previous plan is kept -- same
+ * chunks, CTA assignment, partial blocks and merge index -- with each range's
+ * last unit ending at the new range end and the new causal positions, and
+ * *reused = 1 (fanout_attn then re-uploads only the unit table instead of
+ * planning again); otherwise a new plan, *reused = 0. Outputs and errors as
+ * fanout_plan; `reused` may be NULL. Host only. */
+FANOUT_API int fanout_plan_step(const int32_t *prev_suffix_lens, const int32_t *suffix_lens,
+                const int32_t *q_rows_per_branch, int32_t num_branches, int32_t prefix_len,
+                int32_t H_q, int32_t H_kv, int32_t page_size, int32_t causal, int32_t num_sms,
+                int32_t *units, int32_t cap, int32_t *n_units, int32_t *cta_first,
+                int32_t cta_cap, int32_t *n_ctas, int32_t *n_parts, int32_t *reused);
+
 /* Launches one tiny kernel whose single thread waits on a barrier nothing ever
  * completes, bounded by `limit_ns`; returns FANOUT_ETIMEOUT when the bound
  * fires and the kernel came back (the context stays usable), FANOUT_OK never

@@ -45,6 +45,9 @@ ABI = {
     "fanout_set_profile_events": (ctypes.c_int, [_vp, _vp]),
     "fanout_plan": (ctypes.c_int, [_i32p, _i32p, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32p,
                                    _i32, _i32p, _i32p, _i32, _i32p, _i32p]),
+    "fanout_plan_step": (ctypes.c_int, [_i32p, _i32p, _i32p, _i32, _i32, _i32, _i32, _i32, _i32,
+                                        _i32, _i32p, _i32, _i32p, _i32p, _i32, _i32p, _i32p,
+                                        _i32p]),
     "fanout_selftest_wait_timeout": (ctypes.c_int, [_i64, _vp]),
     "fanout_release": (ctypes.c_int, []),
     "fanout_version": (ctypes.c_char_p, []),
@@ -176,6 +179,26 @@ def plan(suffix_lens, q_rows, prefix_len: int, h_q: int, h_kv: int, page_size: i
                            _ptr(cta), int(cta.shape[0]), ctypes.byref(n_ctas),
                            ctypes.byref(n_parts)), "fanout_plan")
     return units[:n_units.value], cta, int(n_parts.value)
+
+
+def plan_step(prev_suffix_lens, suffix_lens, q_rows, prefix_len: int, h_q: int, h_kv: int,
+              page_size: int, causal: bool, num_sms: int = 148):
+    """The plan fanout_attn runs after a call that differed only in suffix
+    lengths: (units [n, 8], cta_first [n_cta+1], n_parts, reused)."""
+    ps_, sl, tq = _i32arr(prev_suffix_lens), _i32arr(suffix_lens), _i32arr(q_rows)
+    lib = load()
+    n_units, n_ctas, n_parts, reused = (ctypes.c_int32(0) for _ in range(4))
+    args = (_ptr(ps_), _ptr(sl), _ptr(tq), int(sl.shape[0]), int(prefix_len), int(h_q),
+            int(h_kv), int(page_size), int(bool(causal)), int(num_sms))
+    _check(lib.fanout_plan_step(*args, None, 0, ctypes.byref(n_units), None, 0,
+                                ctypes.byref(n_ctas), ctypes.byref(n_parts), None),
+           "fanout_plan_step")
+    units = np.zeros((max(n_units.value, 1), 8), dtype=np.int32)
+    cta = np.zeros(n_ctas.value + 1, dtype=np.int32)
+    _check(lib.fanout_plan_step(*args, _ptr(units), int(units.shape[0]), ctypes.byref(n_units),
+                                _ptr(cta), int(cta.shape[0]), ctypes.byref(n_ctas),
+                                ctypes.byref(n_parts), ctypes.byref(reused)), "fanout_plan_step")
+    return units[:n_units.value], cta, int(n_parts.value), bool(reused.value)
 
 
 def set_option(option: int, value: int) -> None:

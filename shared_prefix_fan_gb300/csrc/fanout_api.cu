@@ -304,6 +304,40 @@ int fanout_plan(const int32_t* suffix_lens, const int32_t* q_rows_per_branch,
     return FANOUT_OK;
 }
 
+int fanout_plan_step(const int32_t* prev_suffix_lens, const int32_t* suffix_lens,
+                     const int32_t* q_rows_per_branch, int32_t num_branches, int32_t prefix_len,
+                     int32_t H_q, int32_t H_kv, int32_t page_size, int32_t causal, int32_t num_sms,
+                     int32_t* units, int32_t cap, int32_t* n_units, int32_t* cta_first,
+                     int32_t cta_cap, int32_t* n_ctas, int32_t* n_parts, int32_t* reused) {
+    int st = validate_shape(prev_suffix_lens, q_rows_per_branch, num_branches, prefix_len, H_q,
+                            H_kv, kHD, page_size, causal);
+    if (st != FANOUT_OK) return st;
+    st = validate_shape(suffix_lens, q_rows_per_branch, num_branches, prefix_len, H_q, H_kv, kHD,
+                        page_size, causal);
+    if (st != FANOUT_OK) return st;
+    if (cap < 0 || (cap > 0 && !units) || cta_cap < 0 || (cta_cap > 0 && !cta_first))
+        return FANOUT_EINVAL;
+    const int32_t sms = num_sms > 0 ? num_sms : 148;
+    PlanInput prev{prev_suffix_lens, q_rows_per_branch, num_branches, prefix_len, H_q, H_kv,
+                   page_size, causal, sms, static_cast<int32_t>(g_force_splits)};
+    PlanInput in{suffix_lens, q_rows_per_branch, num_branches, prefix_len, H_q, H_kv,
+                 page_size, causal, sms, static_cast<int32_t>(g_force_splits)};
+    Plan plan;
+    if ((st = build_plan(prev, plan)) != FANOUT_OK) return st;
+    const bool kept = patch_plan(in, plan);
+    if (!kept && (st = build_plan(in, plan)) != FANOUT_OK) return st;
+    if (reused) *reused = kept ? 1 : 0;
+    const int32_t n = static_cast<int32_t>(plan.units.size());
+    if (n_units) *n_units = n;
+    if (n_ctas) *n_ctas = plan.n_cta();
+    if (n_parts) *n_parts = plan.n_parts;
+    for (int32_t i = 0; i < std::min(n, cap); ++i)
+        std::memcpy(units + 8 * static_cast<int64_t>(i), &plan.units[i], sizeof(Unit));
+    for (int32_t i = 0; i < std::min<int32_t>(static_cast<int32_t>(plan.cta_first.size()), cta_cap); ++i)
+        cta_first[i] = plan.cta_first[i];
+    return FANOUT_OK;
+}
+
 int fanout_attn(const void* q, const void* k_pages, const void* v_pages,
                 const int32_t* page_table, int32_t prefix_len, const int32_t* suffix_lens,
                 const int32_t* q_rows_per_branch, int32_t num_branches,
@@ -352,7 +386,30 @@ int fanout_attn(const void* q, const void* k_pages, const void* v_pages,
                                 static_cast<int32_t>(g_force_splits)};
     key.insert(key.end(), suffix_lens, suffix_lens + num_branches);
     key.insert(key.end(), q_rows_per_branch, q_rows_per_branch + num_branches);
-    if (!ws->plan_ready || key != ws->key) {
+    // A call that differs from the cached plan's only in suffix lengths (a
+    // decode step) keeps the plan when every key range keeps its tile count:
+    // only the unit table moves (new range ends and causal positions).
+    const size_t fixed = 8;  // key entries before the suffix lengths
+    bool patched = false;
+    if (ws->plan_ready && key != ws->key && key.size() == ws->key.size() &&
+        std::equal(key.begin(), key.begin() + fixed, ws->key.begin()) &&
+        std::equal(key.begin() + fixed + num_branches, key.end(),
+                   ws->key.begin() + fixed + num_branches)) {
+        PlanInput in{suffix_lens, q_rows_per_branch, num_branches, prefix_len, H_q, H_kv,
+                     page_size, causal, sms, static_cast<int32_t>(g_force_splits)};
+        if (patch_plan(in, ws->plan)) {
+            ce = cudaMemcpyAsync(static_cast<uint8_t*>(ws->buf) + ws->layout.units,
+                                 ws->plan.units.data(), ws->plan.units.size() * sizeof(Unit),
+                                 cudaMemcpyHostToDevice, stream);
+            if (ce != cudaSuccess) {
+                ws->plan_ready = false;
+                return status_from_cuda(ce);
+            }
+            ws->key = key;
+            patched = true;
+        }
+    }
+    if (!patched && (!ws->plan_ready || key != ws->key)) {
         PlanInput in{suffix_lens, q_rows_per_branch, num_branches, prefix_len, H_q, H_kv,
                      page_size, causal, sms, static_cast<int32_t>(g_force_splits)};
         ws->plan_ready = false;

@@ -46,6 +46,13 @@ struct PlanInput {
     int32_t tail_cuts = 1; // 0: never cut a direct range to even out the last wave
 };
 
+// A key range of the plan: the rows of n_tok tokens from tok_begin (one KV
+// head) against keys [lo, hi) of a branch (branch 0 for the shared prefix).
+struct PlanRange {
+    int32_t kv_head, branch, tok_begin, n_tok, lo, hi, pos_base;
+    bool complete;  // covers every visible key of its rows (no other range does)
+};
+
 struct Plan {
     std::vector<Unit> units;         // grouped by CTA: CTA c runs units [cta_first[c], cta_first[c+1])
     std::vector<int32_t> cta_first;  // n_cta + 1 entries
@@ -60,11 +67,20 @@ struct Plan {
     int32_t tpt = 0;                 // tokens per 128-row query tile
     int32_t nq = 1;                  // query tiles per unit (1 or 2)
     bool need_merge = false;
+    std::vector<PlanRange> ranges;   // the key ranges the units were cut from
+    std::vector<int32_t> unit_range; // per unit: its range
     int32_t n_cta() const { return cta_first.empty() ? 0 : static_cast<int32_t>(cta_first.size()) - 1; }
 };
 
 // Builds the work plan (host only). Returns a fanout_status code.
 int build_plan(const PlanInput& in, Plan& plan);
+
+// Carries `plan` over to a problem that differs from the one it was built
+// for only in suffix lengths, when every key range keeps its number of
+// 128-key tiles: the chunking, CTA assignment, partial blocks and merge index
+// stay; each range's last unit gets the new range end and every unit the new
+// causal position base. Returns false (plan untouched) otherwise.
+bool patch_plan(const PlanInput& in, Plan& plan);
 
 struct MergeParams {
     const float* part_o;

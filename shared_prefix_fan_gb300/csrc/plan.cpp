@@ -40,10 +40,7 @@
 namespace fanout {
 namespace {
 
-struct Range {
-    int32_t kv_head, branch, tok_begin, n_tok, lo, hi, pos_base;
-    bool complete;  // covers every visible key of its rows (no other range does)
-};
+using Range = PlanRange;
 
 inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -59,6 +56,7 @@ struct Cand {
     std::vector<Unit> units;   // in assignment order
     std::vector<int64_t> work;
     std::vector<int32_t> cta_of;
+    std::vector<int32_t> range_of;
     int32_t n_cta = 0;
     double cost = 0;
 };
@@ -70,9 +68,11 @@ void make_candidate(const std::vector<Range>& ranges, int64_t chunk, int32_t for
         int64_t work;
         Unit u;
         bool whole;
+        int32_t range;
     };
     std::vector<Keyed> all;
-    for (const Range& r : ranges) {
+    for (size_t ri = 0; ri < ranges.size(); ++ri) {
+        const Range& r = ranges[ri];
         const int64_t nkt = cdiv(r.hi - r.lo, kBN);
         int64_t nch = force_splits > 0 ? force_splits : (chunk > 0 ? cdiv(nkt, chunk) : 1);
         nch = std::max<int64_t>(1, std::min(nch, nkt));
@@ -83,7 +83,7 @@ void make_candidate(const std::vector<Range>& ranges, int64_t chunk, int32_t for
             all.push_back({t_hi - t_lo,
                            Unit{r.kv_head, r.branch, r.tok_begin, r.n_tok, k_lo, k_hi, r.pos_base,
                                 0},
-                           r.complete && nch == 1});
+                           r.complete && nch == 1, static_cast<int32_t>(ri)});
         }
     }
     std::stable_sort(all.begin(), all.end(), [](const Keyed& a, const Keyed& b) {
@@ -94,6 +94,7 @@ void make_candidate(const std::vector<Range>& ranges, int64_t chunk, int32_t for
     c.units.clear();
     c.work.clear();
     c.cta_of.clear();
+    c.range_of.clear();
     using Slot = std::pair<double, int32_t>;
     std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
     for (int32_t i = 0; i < c.n_cta; ++i) heap.push({0.0, i});
@@ -111,6 +112,7 @@ void make_candidate(const std::vector<Range>& ranges, int64_t chunk, int32_t for
         c.units.push_back(u);
         c.work.push_back(k.work);
         c.cta_of.push_back(s.second);
+        c.range_of.push_back(k.range);
     }
     c.cost = makespan + (n_parts > 0 ? kMergeLaunch + kMergePerPart * n_parts / c.n_cta : 0.0);
 }
@@ -129,10 +131,12 @@ void make_streamk(const std::vector<Range>& ranges, int32_t max_cta, double unit
     c.units.clear();
     c.work.clear();
     c.cta_of.clear();
+    c.range_of.clear();
     std::vector<double> load(n_cta, 0.0);
     int32_t cta = 0;
     int64_t n_parts = 0;
-    for (const Range& r : ranges) {
+    for (size_t ri = 0; ri < ranges.size(); ++ri) {
+        const Range& r = ranges[ri];
         const int64_t nkt = cdiv(r.hi - r.lo, kBN);
         int64_t t = 0;
         while (t < nkt) {
@@ -152,6 +156,7 @@ void make_streamk(const std::vector<Range>& ranges, int32_t max_cta, double unit
             if (!whole) ++n_parts;
             c.work.push_back(take);
             c.cta_of.push_back(cta);
+            c.range_of.push_back(static_cast<int32_t>(ri));
             load[cta] += static_cast<double>(take) + unit_ovh;
             t += take;
         }
@@ -198,8 +203,9 @@ void make_lpt_cut(const std::vector<Range>& ranges, int32_t max_cta, double unit
     c.units.clear();
     c.work.clear();
     c.cta_of.clear();
+    c.range_of.clear();
     std::vector<bool> cut(ranges.size(), false);
-    std::vector<int32_t> range_of;
+    std::vector<int32_t>& range_of = c.range_of;
     double makespan = 0;
     while (!queue.empty()) {
         Piece pc = queue.top();
@@ -245,10 +251,11 @@ void make_lpt_cut(const std::vector<Range>& ranges, int32_t max_cta, double unit
     c.cost = makespan + (n_parts > 0 ? kMergeLaunch + kMergePerPart * n_parts / c.n_cta : 0.0);
 }
 
-}  // namespace
-
-int build_plan(const PlanInput& in, Plan& plan) {
-    plan = Plan();
+// The key ranges of a problem (rows x keys before any split-KV cut), and the
+// row geometry: R tokens, nq query tiles per unit, tpt tokens per tile.
+void make_ranges(const PlanInput& in, std::vector<Range>& ranges, int32_t& R, int32_t& nq,
+                 int32_t& tpt_tile) {
+    ranges.clear();
     const int32_t B = in.num_branches;
     // A prefix that ends inside a page: the whole pages are the shared range;
     // the tail of the last prefix page is read through each branch's own table
@@ -267,18 +274,14 @@ int build_plan(const PlanInput& in, Plan& plan) {
         if (in.q_rows[b] > 0) ++active;
         max_t = std::max(max_t, in.q_rows[b]);
     }
-    const int32_t R = tok0[B];
-    plan.R = R;
-    if (R == 0) return 0;
+    R = tok0[B];
     const bool shared = active >= 2 && P > 0;
     // Two 128-row query tiles per unit when the row blocks are long enough to
     // fill them (they then share every K/V tile); one otherwise.
     const int64_t block_rows = static_cast<int64_t>(shared ? R : max_t) * G;
-    plan.nq = block_rows > kBM ? 2 : 1;
-    plan.tpt = kBM / G;
-    const int32_t tpt = plan.tpt * plan.nq;  // tokens per unit
-
-    std::vector<Range> ranges;
+    nq = block_rows > kBM ? 2 : 1;
+    tpt_tile = kBM / G;
+    const int32_t tpt = tpt_tile * nq;  // tokens per unit
     for (int32_t h = 0; h < in.H_kv; ++h) {
         if (shared) {
             for (int32_t t = 0; t < R; t += tpt)
@@ -299,6 +302,23 @@ int build_plan(const PlanInput& in, Plan& plan) {
             }
         }
     }
+}
+
+}  // namespace
+
+int build_plan(const PlanInput& in, Plan& plan) {
+    plan = Plan();
+    const int32_t B = in.num_branches;
+    std::vector<Range> ranges;
+    int32_t R = 0;
+    make_ranges(in, ranges, R, plan.nq, plan.tpt);
+    plan.R = R;
+    if (R == 0) return 0;
+    const int32_t G = in.H_q / in.H_kv;
+    std::vector<int32_t> S_eff(B);
+    const int32_t tail = in.prefix_len % in.page_size;
+    const int32_t P = in.prefix_len - tail;
+    for (int32_t b = 0; b < B; ++b) S_eff[b] = in.suffix_lens[b] + tail;
 
     // Chunk size from the cost model (or the forced split count).
     const int32_t max_cta = std::max(1, in.num_sms);
@@ -358,8 +378,13 @@ int build_plan(const PlanInput& in, Plan& plan) {
     for (int32_t c = 0; c < n_cta; ++c) plan.cta_first[c + 1] += plan.cta_first[c];
     std::vector<int32_t> fill(plan.cta_first.begin(), plan.cta_first.end() - 1);
     plan.units.resize(best.units.size());
-    for (size_t i = 0; i < best.units.size(); ++i)
-        plan.units[fill[best.cta_of[i]]++] = best.units[i];
+    plan.unit_range.resize(best.units.size());
+    for (size_t i = 0; i < best.units.size(); ++i) {
+        const int32_t at = fill[best.cta_of[i]]++;
+        plan.units[at] = best.units[i];
+        plan.unit_range[at] = best.range_of[i];
+    }
+    plan.ranges = ranges;
     int32_t n_parts = 0;
     for (Unit& u : plan.units)
         if (u.part >= 0) u.part = n_parts++;
@@ -397,6 +422,33 @@ int build_plan(const PlanInput& in, Plan& plan) {
     }
     plan.need_merge = n_parts > 0;
     return 0;
+}
+
+bool patch_plan(const PlanInput& in, Plan& plan) {
+    if (plan.units.empty() || plan.unit_range.size() != plan.units.size()) return false;
+    std::vector<Range> ranges;
+    int32_t R = 0, nq = 0, tpt = 0;
+    make_ranges(in, ranges, R, nq, tpt);
+    if (R != plan.R || nq != plan.nq || tpt != plan.tpt || ranges.size() != plan.ranges.size())
+        return false;
+    for (size_t i = 0; i < ranges.size(); ++i) {
+        const Range& a = ranges[i];
+        const Range& o = plan.ranges[i];
+        if (a.kv_head != o.kv_head || a.branch != o.branch || a.tok_begin != o.tok_begin ||
+            a.n_tok != o.n_tok || a.lo != o.lo || a.complete != o.complete ||
+            (a.pos_base == kNoCausal) != (o.pos_base == kNoCausal) ||
+            cdiv(a.hi - a.lo, kBN) != cdiv(o.hi - o.lo, kBN))
+            return false;
+    }
+    for (size_t k = 0; k < plan.units.size(); ++k) {
+        Unit& u = plan.units[k];
+        const Range& o = plan.ranges[plan.unit_range[k]];
+        const Range& a = ranges[plan.unit_range[k]];
+        if (u.key_end == o.hi) u.key_end = a.hi;  // the range's last unit
+        u.pos_base = a.pos_base;
+    }
+    plan.ranges = ranges;
+    return true;
 }
 
 }  // namespace fanout

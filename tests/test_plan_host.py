@@ -17,8 +17,13 @@ def _built():
 
 
 def check_plan(S, T, P, h_q, h_kv, ps, causal, sms=148):
+    units, cta_first, n_parts = binding.plan(list(map(int, S)), list(map(int, T)), P, h_q, h_kv,
+                                             ps, causal, sms)
+    return check_units(units, cta_first, n_parts, S, T, P, h_q, h_kv, ps, causal, sms)
+
+
+def check_units(units, cta_first, n_parts, S, T, P, h_q, h_kv, ps, causal, sms=148):
     S, T = list(map(int, S)), list(map(int, T))
-    units, cta_first, n_parts = binding.plan(S, T, P, h_q, h_kv, ps, causal, sms)
     G = h_q // h_kv
     R = sum(T)
     n_cta = len(cta_first) - 1
@@ -145,3 +150,63 @@ def test_plan_decode_unit_counts():
     units, cta, _ = check_plan(w.suffix_lens, w.q_rows, s.prefix_len, s.h_q, s.h_kv,
                                s.page_size, s.causal, sms=152)
     assert np.diff(cta).max() <= 2
+
+
+
+def test_plan_step_keeps_plan_for_a_decode_step():
+    """A decode step (every suffix one token longer, no key range gaining a
+    128-key tile) keeps the previous plan's chunks and CTA assignment; only
+    the range ends and causal positions move, and the plan stays a complete,
+    disjoint cover of every visible key."""
+    w = draw(WORKLOADS["decode"])
+    s = w.spec
+    S0 = [500] * 8                      # 4 tiles of suffix keys per branch
+    S1 = [501] * 8
+    prev, prev_cta, prev_parts = binding.plan(S0, w.q_rows, s.prefix_len, s.h_q, s.h_kv,
+                                              s.page_size, s.causal, 152)
+    units, cta, n_parts, reused = binding.plan_step(S0, S1, w.q_rows, s.prefix_len, s.h_q, s.h_kv,
+                                                    s.page_size, s.causal, 152)
+    assert reused
+    assert (cta == prev_cta).all() and n_parts == prev_parts
+    same = [0, 1, 2, 3, 4, 7]           # kv_head, branch, tok_begin, n_tok, key_begin, part
+    assert (units[:, same] == prev[:, same]).all()
+    check_units(units, cta, n_parts, S1, w.q_rows, s.prefix_len, s.h_q, s.h_kv, s.page_size,
+                s.causal, 152)
+
+
+def test_plan_step_replans_when_a_range_gains_a_tile():
+    w = draw(WORKLOADS["decode"])
+    s = w.spec
+    S0, S1 = [512] * 8, [513] * 8        # 4 -> 5 tiles of suffix keys
+    units, cta, n_parts, reused = binding.plan_step(S0, S1, w.q_rows, s.prefix_len, s.h_q, s.h_kv,
+                                                    s.page_size, s.causal, 152)
+    assert not reused
+    fresh, fresh_cta, fresh_parts = binding.plan(S1, w.q_rows, s.prefix_len, s.h_q, s.h_kv,
+                                                 s.page_size, s.causal, 152)
+    assert (units == fresh).all() and (cta == fresh_cta).all() and n_parts == fresh_parts
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_plan_step_random(seed):
+    """Random problems and random suffix growth: a kept plan is a valid plan of
+    the new problem with the old structure; a rebuilt one is the fresh plan."""
+    rng = np.random.default_rng(1000 + seed)
+    B = int(rng.integers(1, 6))
+    ps = int(rng.choice([16, 32, 64, 128]))
+    P = ps * int(rng.integers(0, 12)) + (int(rng.integers(1, ps)) if seed % 3 == 2 else 0)
+    causal = bool(rng.integers(0, 2))
+    T = rng.integers(0, 30, size=B)
+    S0 = np.array([int(t) + int(rng.integers(0 if P else 1, 400)) for t in T])
+    S1 = S0 + rng.integers(0, 3 if seed % 2 == 0 else 300, size=B)
+    hkv = int(rng.choice([1, 2, 8]))
+    hq = hkv * int(rng.choice([1, 4, 8, 16]))
+    sms = int(rng.choice([7, 148]))
+    units, cta, n_parts, reused = binding.plan_step(S0, S1, T, P, hq, hkv, ps, causal, sms)
+    check_units(units, cta, n_parts, S1, T, P, hq, hkv, ps, causal, sms)
+    if reused:
+        prev, prev_cta, _ = binding.plan(S0, T, P, hq, hkv, ps, causal, sms)
+        assert (cta == prev_cta).all()
+        assert (units[:, [0, 1, 2, 3, 4, 7]] == prev[:, [0, 1, 2, 3, 4, 7]]).all()
+    else:
+        fresh, fresh_cta, _ = binding.plan(S1, T, P, hq, hkv, ps, causal, sms)
+        assert (units == fresh).all() and (cta == fresh_cta).all()
