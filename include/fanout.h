@@ -325,7 +325,9 @@ FANOUT_API int fanout_selftest_wait_timeout(int64_t limit_ns, fanout_stream_t st
  *     that overlap on the GPU (two streams, or a new call before the previous
  *     one finished) race on it and corrupt each other's results;
  *   - FANOUT_OPT_WAIT_LIMIT_NS and FANOUT_OPT_NUM_SMS do not apply (1 s bound,
- *     the device's own SM count); profile events are not recorded.
+ *     the device's own SM count); profile events are not recorded;
+ *   - the last plan is kept per device (not per stream), and reused or
+ *     carried over to new suffix lengths as fanout_plan_step describes.
  */
 #define FANOUT_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
 FANOUT_API int fanout_attn_noalloc(const void *q, const void *k_pages, const void *v_pages,

@@ -28,8 +28,10 @@
 // array and corrupt each other's results.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <mutex>
+#include <vector>
 
 #include "../../include/fanout.h"
 #include "fanout_internal.h"
@@ -45,6 +47,16 @@ constexpr int kMaxDevices = 64;
 std::mutex g_setup_mu;
 void* g_scratch_addr[kMaxDevices] = {};
 uint32_t g_epoch[kMaxDevices] = {};  // fused-merge flag value of the last call per device
+
+// The last plan per device (host memory; guarded by g_setup_mu), kept for a
+// call with the same problem, or carried over to one whose suffix lengths
+// alone changed (patch_plan), as fanout_attn does per stream.
+struct PlanCache {
+    std::vector<int32_t> key;
+    Plan plan;
+    bool ready = false;
+};
+PlanCache g_plan_cache[kMaxDevices];
 
 // Once per device, with that device current: the device address of the array.
 int scratch_for_device(int dev, uint8_t** out) {
@@ -83,19 +95,54 @@ extern "C" FANOUT_API int fanout_attn_noalloc(
     if (cudaGetDevice(&dev) != cudaSuccess) return FANOUT_ECUDA;
     int sms = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    // The same plan fanout_attn builds (host memory only).
-    Plan plan;
+    // The same plan fanout_attn builds (host memory only): the device's last
+    // plan when the problem is the same or only its suffix lengths moved
+    // within their tiles, else a new one.
+    if (dev < 0 || dev >= kMaxDevices) return FANOUT_EUNSUPPORTED;
     PlanInput in{suffix_lens, q_rows_per_branch, num_branches, prefix_len, H_q, H_kv,
                  page_size, causal, sms > 0 ? sms : 1, current_force_splits()};
-    if ((st = build_plan(in, plan)) != FANOUT_OK) return st;
-    Layout L = plan_layout(plan);
-    if (L.total > kScratchBytes) {
-        // without the tail cuts a long prefill has no partials at all
-        in.tail_cuts = 0;
+    std::vector<int32_t> key = {prefix_len, num_branches, H_q, H_kv, page_size, causal, in.num_sms,
+                                in.force_splits};
+    const size_t fixed = key.size();
+    key.insert(key.end(), suffix_lens, suffix_lens + num_branches);
+    key.insert(key.end(), q_rows_per_branch, q_rows_per_branch + num_branches);
+    Plan plan;
+    bool have = false;
+    {
+        std::lock_guard<std::mutex> lk(g_setup_mu);
+        PlanCache& c = g_plan_cache[dev];
+        if (c.ready && c.key == key) {
+            plan = c.plan;
+            have = true;
+        } else if (c.ready && c.key.size() == key.size() &&
+                   std::equal(key.begin(), key.begin() + fixed, c.key.begin()) &&
+                   std::equal(key.begin() + fixed + num_branches, key.end(),
+                              c.key.begin() + fixed + num_branches)) {
+            plan = c.plan;
+            have = patch_plan(in, plan);
+        }
+    }
+    Layout L;
+    if (have) {
+        L = plan_layout(plan);
+    } else {
         if ((st = build_plan(in, plan)) != FANOUT_OK) return st;
         L = plan_layout(plan);
+        if (L.total > kScratchBytes) {
+            // without the tail cuts a long prefill has no partials at all
+            in.tail_cuts = 0;
+            if ((st = build_plan(in, plan)) != FANOUT_OK) return st;
+            L = plan_layout(plan);
+        }
     }
     if (L.total > kScratchBytes) return FANOUT_ENOMEM;  // beyond the fixed array
+    {
+        std::lock_guard<std::mutex> lk(g_setup_mu);
+        PlanCache& c = g_plan_cache[dev];
+        c.key = key;
+        c.plan = plan;
+        c.ready = true;
+    }
 
     uint8_t* scratch = nullptr;
     if ((st = scratch_for_device(dev, &scratch)) != FANOUT_OK) return st;

@@ -69,3 +69,32 @@ def test_noalloc_long_prefill():
     assert _noalloc(dw, out, lse) == binding.OK
     assert binding.last_error() == binding.OK
     _close(out, lse, ref_out, ref_lse)
+
+
+def test_noalloc_decode_steps():
+    """Decode steps through the no-allocation entry: it keeps the device's last
+    plan while the suffix lengths move within their tiles (and plans anew when
+    a range gains a tile); every step matches the fp64 oracle."""
+    import dataclasses
+
+    import oracle
+    from shared_prefix_fan_gb300.workloads import small_spec
+    from tests.gpu_helpers import compare
+
+    S0 = np.array([100, 90, 110, 100], dtype=np.int32)
+    grows = [0, 1, 2, 7, 40]
+    spec = small_spec(h_q=64, h_kv=8, page_size=64, prefix_len=2048, q_rows=[1, 1, 1, 1],
+                      suffix_lens=[int(x) for x in S0 + max(grows)], permute_prefix=True,
+                      permute_suffix=True, seed=78)
+    dw = DevWorkload(draw(spec))
+    w_max = dw.w
+    for grow in grows:
+        S = S0 + grow
+        dw.w = dataclasses.replace(w_max, suffix_lens=S)
+        out = torch.full((dw.w.total_rows, spec.h_q, 128), float("nan"), device="cuda")
+        lse = torch.full((dw.w.total_rows, spec.h_q), float("nan"), device="cuda")
+        assert _noalloc(dw, out, lse) == binding.OK
+        assert binding.last_error() == binding.OK
+        ref = oracle.attn(dw.w.q, dw.w.k_pool, dw.w.v_pool, dw.table_host, spec.prefix_len, S,
+                          dw.w.q_rows, spec.h_q, spec.h_kv, spec.page_size, spec.scale, spec.causal)
+        compare(out, lse, *ref, what=f"no-alloc step +{grow}")
