@@ -117,6 +117,30 @@ void make_candidate(const std::vector<Range>& ranges, int64_t chunk, int32_t for
     c.cost = makespan + (n_parts > 0 ? kMergeLaunch + kMergePerPart * n_parts / c.n_cta : 0.0);
 }
 
+// A lower bound of make_candidate's cost for chunk size `chunk` (whole-range
+// chunking when 0), from the pieces' sizes alone: the busiest CTA carries at
+// least the largest piece and at least the average load. A candidate whose
+// bound cannot beat the best so far is skipped without being built.
+double candidate_cost_bound(const std::vector<Range>& ranges, int64_t chunk, int32_t max_cta,
+                            double unit_ovh) {
+    int64_t n = 0, n_parts = 0, total = 0, max_w = 0;
+    for (const Range& r : ranges) {
+        const int64_t nkt = cdiv(r.hi - r.lo, kBN);
+        int64_t nch = chunk > 0 ? cdiv(nkt, chunk) : 1;
+        nch = std::max<int64_t>(1, std::min(nch, nkt));
+        for (int64_t ch = 0; ch < nch; ++ch)
+            max_w = std::max(max_w, (ch + 1) * nkt / nch - ch * nkt / nch);
+        total += nkt;
+        n += nch;
+        if (!(r.complete && nch == 1)) n_parts += nch;
+    }
+    const int32_t n_cta = static_cast<int32_t>(std::min<int64_t>(max_cta, n));
+    const double makespan =
+        std::max(static_cast<double>(max_w) + unit_ovh,
+                 (static_cast<double>(total) + unit_ovh * static_cast<double>(n)) / n_cta);
+    return makespan + (n_parts > 0 ? kMergeLaunch + kMergePerPart * n_parts / n_cta : 0.0);
+}
+
 // Exact-balance candidate (Stream-K style): the ranges' tiles laid end to end
 // and cut into one contiguous quota per CTA; a CTA's quota may end inside a
 // range and the next CTA continues it.
@@ -342,6 +366,8 @@ int build_plan(const PlanInput& in, Plan& plan) {
                 for (const Range& r : ranges) n += cdiv(cdiv(r.hi - r.lo, kBN), chunk);
                 if (n > max_units) continue;
             }
+            if (!first && candidate_cost_bound(ranges, chunk, max_cta, ovh) >= best.cost * 0.995)
+                continue;  // could not replace the best
             make_candidate(ranges, chunk, 0, max_cta, ovh, cand);
             if (first || cand.cost < best.cost * 0.995) {
                 std::swap(best, cand);
