@@ -202,6 +202,8 @@ void make_lpt_cut(const std::vector<Range>& ranges, int32_t max_cta, double unit
         int64_t work;
         int32_t range;
         int64_t t_lo;  // first tile of the piece within its range
+        // the queue's order after the size: first key, KV head, branch, token
+        int32_t k_lo, kv_head, branch, tok_begin;
     };
     int64_t total = 0;
     std::vector<int64_t> nkt(ranges.size());
@@ -212,15 +214,18 @@ void make_lpt_cut(const std::vector<Range>& ranges, int32_t max_cta, double unit
     const int32_t n_cta = static_cast<int32_t>(std::min<int64_t>(max_cta, total));
     const double target = (static_cast<double>(total) +
                            unit_ovh * static_cast<double>(ranges.size() + n_cta)) / n_cta;
-    auto key = [&](const Piece& a) {
-        const Range& r = ranges[a.range];
-        return std::make_tuple(-a.work, r.lo + static_cast<int32_t>(a.t_lo) * kBN, r.kv_head,
-                               r.branch, r.tok_begin);
+    auto later = [](const Piece& a, const Piece& b) {
+        return std::make_tuple(-b.work, b.k_lo, b.kv_head, b.branch, b.tok_begin) <
+               std::make_tuple(-a.work, a.k_lo, a.kv_head, a.branch, a.tok_begin);
     };
-    auto later = [&](const Piece& a, const Piece& b) { return key(b) < key(a); };
+    auto piece = [&](int64_t work, int32_t ri, int64_t t_lo) {
+        const Range& r = ranges[ri];
+        return Piece{work, ri, t_lo, r.lo + static_cast<int32_t>(t_lo) * kBN, r.kv_head, r.branch,
+                     r.tok_begin};
+    };
     std::priority_queue<Piece, std::vector<Piece>, decltype(later)> queue(later);
     for (size_t i = 0; i < ranges.size(); ++i)
-        if (nkt[i] > 0) queue.push(Piece{nkt[i], static_cast<int32_t>(i), 0});
+        if (nkt[i] > 0) queue.push(piece(nkt[i], static_cast<int32_t>(i), 0));
     using Slot = std::pair<double, int32_t>;
     std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
     for (int32_t i = 0; i < n_cta; ++i) heap.push({0.0, i});
@@ -241,7 +246,7 @@ void make_lpt_cut(const std::vector<Range>& ranges, int32_t max_cta, double unit
         if (s.first + unit_ovh + static_cast<double>(pc.work) > target + 0.5 && room >= 1.0 &&
             pc.work >= 2) {
             take = std::min<int64_t>(pc.work - 1, static_cast<int64_t>(room));
-            queue.push(Piece{pc.work - take, pc.range, pc.t_lo + take});
+            queue.push(piece(pc.work - take, pc.range, pc.t_lo + take));
             cut[pc.range] = true;
         }
         const Range& r = ranges[pc.range];
