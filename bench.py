@@ -8,7 +8,11 @@ workload is the fan-out decode configuration (H_q=64, H_kv=8, d=128;
 branch; page 64; split-KV 32 ways). Prints ONE JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
-                  [--impl gpu|reference]
+                  [--per-config all|none|a,b] [--impl gpu|reference]
+
+The line's top-level value, roofline, cpu_baseline, e2e and clocks are those
+of --config (decode by default); "per_config" holds the same measurements for
+each of the five workloads (tiny, decode, batching, wide, prefill).
 
 Under torchrun (N > 1) every rank runs an independent replica of the same
 problem on its own GPU (the path has no exchange step); timing is the max
@@ -103,6 +107,21 @@ def ncu_traffic(workload: str):
     if not d or d.get("source_sha") != kernel_source_sha():
         return None
     return float(d["dram_bytes_per_launch"])
+
+
+L2_NOTE = ("GPU arm: L2 flushed between timed calls (write 2x L2, then read 2x L2); "
+           "CPU oracle arm: no device cache involved")
+
+
+def workload_config(w, world: int) -> dict:
+    """The `config` object of a line: the workload and its sizes only, the same
+    in the GPU and the reference arm."""
+    s = w.spec
+    return {"workload": s.name, "h_q": s.h_q, "h_kv": s.h_kv, "d": s.d,
+            "branches": w.num_branches, "q_rows": int(w.total_rows),
+            "prefix_len": s.prefix_len, "suffix_tokens": int(w.suffix_lens.sum()),
+            "page_size": s.page_size, "causal": s.causal, "l2": L2_NOTE,
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
 
 
 # ------------------------------------------------------------------ clocks
@@ -217,8 +236,10 @@ def _row_keys(w):
 
 
 def run_reference(args):
-    """Reference arm: the fp64 CPU oracle, timed on this host's cores."""
+    """Reference arm: the fp64 CPU oracle as it stands, timed on this host's
+    cores on bounded samples of the same workloads (rank 0 only)."""
     rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
     if rank != 0:
         return
     w = draw(WORKLOADS[args.config])
@@ -230,17 +251,32 @@ def run_reference(args):
         if i >= args.warmup:
             per_step.append(info[0])
     v = float(np.mean(per_step))
+
+    def cpu_of(value, info_, what):
+        return {"value": value, "unit": "us/call", "cores": info_[3], "kind": "oracle",
+                "sample": f"{info_[2]} of {what.total_rows} query tokens (all heads) "
+                          f"x {info_[4]} repetitions, {info_[1]:.1f} s per step, "
+                          f"extrapolated by visible keys"}
+
+    per = {}
+    for name in parse_per_config(args.per_config):
+        if name == args.config:
+            per[name] = {"value": v, "unit": "us/call", "config": workload_config(w, world),
+                         "cpu_baseline": cpu_of(v, info, w)}
+            continue
+        wn = draw(WORKLOADS[name])
+        inf = oracle_sample(wn, budget_s=5.0)
+        per[name] = {"value": inf[0], "unit": "us/call", "config": workload_config(wn, world),
+                     "cpu_baseline": cpu_of(inf[0], inf, wn)}
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "us/call",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": v / 1e3, "higher_is_better": False, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.config},
-            "cpu_baseline": {"value": v, "unit": "us/call", "cores": info[3], "kind": "oracle",
-                             "sample": f"{info[2]} of {w.total_rows} query tokens (all heads) "
-                                       f"x {info[4]} repetitions, {info[1]:.1f} s per step, "
-                                       f"extrapolated by visible keys"},
+            "config": workload_config(w, world),
+            "cpu_baseline": cpu_of(v, info, w),
             "e2e": {"value": v, "unit": "us/call", "h2d_bytes_per_step": 0,
-                    "d2h_bytes_per_step": 0}}
+                    "d2h_bytes_per_step": 0},
+            "per_config": {n: per[n] for n in PER_CONFIG_ORDER if n in per}}
     print(json.dumps(line), flush=True)
 
 
@@ -260,12 +296,195 @@ def max_over_ranks(values, dist=None, device="cpu"):
 
 
 # ------------------------------------------------------------------ GPU arm
+def roofline_of(work, peaks, t_kernel_s, workload):
+    """Roofline object of the attention kernel: the slower of its algorithmic
+    bytes (unique KV + Q) at the measured HBM peak and its flops at the
+    measured bf16 peak decides the bound."""
+    t_hbm = work["split_bytes"] / (peaks["hbm"] * 1e9)
+    t_tc = work["flops"] / (peaks["tc"] * 1e12)
+    if t_hbm >= t_tc:
+        achieved = work["split_bytes"] / t_kernel_s / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm"], "unit": "GB/s"}
+    else:
+        achieved = work["flops"] / t_kernel_s / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["tc"], "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = ncu_traffic(workload)
+    roof["algorithmic_bytes"] = work["split_bytes"]
+    roof["algorithmic_flops"] = work["flops"]
+    roof["kernel"] = "attn_fwd_kernel"
+    roof["peak_source"] = f"{peaks['source']} (MEASURED_PEAKS.json burst figure)" \
+        if peaks["source"] == "measured" else "fallback"
+    return roof
+
+
+class Bench:
+    """One GPU (one rank): inputs resident in HBM, the L2 flushed between timed
+    calls (write a buffer twice the L2 size, then read another one, so no dirty
+    line is left to be written back inside the next timed call)."""
+
+    def __init__(self, torch, binding, local, world, dist):
+        self.torch, self.binding, self.local, self.world, self.dist = \
+            torch, binding, local, world, dist
+        l2 = torch.cuda.get_device_properties(local).L2_cache_size
+        n = max(2 * l2, 256 << 20)
+        self.flush_w = torch.empty(n, dtype=torch.uint8, device="cuda")
+        self.flush_r = torch.ones(n // 4, dtype=torch.float32, device="cuda")
+        self.sms = torch.cuda.get_device_properties(local).multi_processor_count
+
+    def flush_l2(self):
+        self.flush_w.zero_()
+        self.flush_r.sum()
+
+    def max_ranks(self, vals):
+        return max_over_ranks(vals, self.dist if self.world > 1 else None, "cuda")
+
+    def run(self, name, steps, warmup, soak_s, e2e_steps, cpu_budget_s):
+        torch, binding = self.torch, self.binding
+        w = draw(WORKLOADS[name])
+        s = w.spec
+        table = binding.fork(w.prefix_pages, w.suffix_lens, s.page_size, w.free_pages,
+                             w.max_pages_per_branch)
+
+        def host_bf16(bits):
+            return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+
+        h_q, h_k, h_v = host_bf16(w.q), host_bf16(w.k_pool), host_bf16(w.v_pool)
+        h_t = torch.from_numpy(table)
+        q, k, v, t = (x.cuda() for x in (h_q, h_k, h_v, h_t))
+        R = w.total_rows
+        out = torch.empty((R, s.h_q, s.d), dtype=torch.float32, device="cuda")
+        lse = torch.empty((R, s.h_q), dtype=torch.float32, device="cuda")
+
+        def call():
+            binding.attn(q, k, v, t, s.prefix_len, w.suffix_lens, w.q_rows, s.h_q, s.h_kv,
+                         s.page_size, s.scale, s.causal, out=out, lse=lse)
+
+        for _ in range(max(3, warmup)):
+            self.flush_l2()
+            call()
+        torch.cuda.synchronize()
+        rc = binding.last_error()
+        if rc != binding.OK:
+            raise RuntimeError(f"{name}: device error {binding.strerror(rc)}")
+        units, cta_first, n_parts = binding.plan(
+            w.suffix_lens, w.q_rows, s.prefix_len, s.h_q, s.h_kv, s.page_size, s.causal,
+            self.sms)
+        launches_per_call = 1 + (1 if n_parts > 0 else 0)
+
+        sampler = ClockSampler(gpu_id_for_smi(torch, self.local))
+        t_end = time.perf_counter() + soak_s
+        while time.perf_counter() < t_end:   # untimed soak: clocks settle and get sampled
+            self.flush_l2()
+            call()
+            torch.cuda.synchronize()
+        stream = torch.cuda.current_stream()
+        ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4)) for _ in range(steps)]
+        for quad in ev:              # the raw CUDA events are created at first record
+            for e in quad:
+                e.record(stream)
+        torch.cuda.synchronize()
+        if self.world > 1:
+            self.dist.barrier()
+        torch.cuda.synchronize()
+        for e0, e1, _, _ in ev:
+            self.flush_l2()                    # L2 flushed between timed calls
+            e0.record(stream)
+            call()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        if self.world > 1:
+            self.dist.barrier()
+        clocks = sampler.stop()
+        # The attention kernel alone, in a second pass: events recorded between it
+        # and a separate merge launch would stop the merge from overlapping it, so
+        # they stay out of the pass the call time comes from.
+        for _, _, k0, k1 in ev:
+            self.flush_l2()
+            binding.set_profile_events(k0, k1)  # brackets the split-KV kernel alone
+            call()
+        torch.cuda.synchronize()
+        binding.set_profile_events(None, None)
+        call_ms = np.array([a.elapsed_time(b) for a, b, _, _ in ev])
+        split_ms = np.array([a.elapsed_time(b) for _, _, a, b in ev])
+        rc = binding.last_error()
+        if rc != binding.OK:
+            raise RuntimeError(f"{name}: device error {binding.strerror(rc)}")
+        mean_call, mean_split = self.max_ranks([float(call_ms.mean()), float(split_ms.mean())])
+
+        # end to end: inputs from pinned host memory, result read back, every step
+        e2e = None
+        if e2e_steps > 0:
+            p_q, p_k, p_v, p_t = (x.pin_memory() for x in (h_q, h_k, h_v, h_t))
+            p_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+            p_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+            e2e_ms = []
+            for i in range(e2e_steps + 2):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                self.flush_l2()
+                a.record(stream)
+                q.copy_(p_q, non_blocking=True)
+                k.copy_(p_k, non_blocking=True)
+                v.copy_(p_v, non_blocking=True)
+                t.copy_(p_t, non_blocking=True)
+                call()
+                p_out.copy_(out, non_blocking=True)
+                p_lse.copy_(lse, non_blocking=True)
+                b.record(stream)
+                torch.cuda.synchronize()
+                if i >= 2:
+                    e2e_ms.append(a.elapsed_time(b))
+            e2e_val = self.max_ranks([float(np.mean(e2e_ms)) * 1e3])[0]
+            h2d = sum(x.numel() * x.element_size() for x in (p_q, p_k, p_v, p_t))
+            d2h = sum(x.numel() * x.element_size() for x in (p_out, p_lse))
+            e2e = {"value": e2e_val, "unit": "us/call", "h2d_bytes_per_step": int(h2d),
+                   "d2h_bytes_per_step": int(d2h), "steps": e2e_steps,
+                   "note": "q, K/V page pool and page table copied from pinned host memory, "
+                           "out and lse copied back, every step"}
+            del p_q, p_k, p_v, p_t, p_out, p_lse
+
+        work = algorithmic_work(w)
+        peaks = load_peaks()
+        roof = roofline_of(work, peaks, mean_split * 1e-3, name)
+        t_call_roof = max(work["call_bytes"] / (peaks["hbm"] * 1e9),
+                          work["flops"] / (peaks["tc"] * 1e12))
+        value_us = mean_call * 1e3
+        cpu = None
+        if cpu_budget_s > 0 and int(os.environ.get("RANK", "0")) == 0:
+            us, dt, nrows, threads, reps = oracle_sample(w, budget_s=cpu_budget_s)
+            cpu = {"value": us, "unit": "us/call", "cores": threads, "kind": "oracle",
+                   "sample": f"{nrows} of {R} query tokens (all {s.h_q} heads) x {reps} "
+                             f"repetitions, {dt:.1f} s, extrapolated to the full call by "
+                             f"visible keys"}
+        entry = {
+            "value": value_us, "unit": "us/call", "steps": steps,
+            "kernel_us": mean_split * 1e3,
+            "config": workload_config(w, self.world),
+            "plan": {"work_units": int(len(units)), "persistent_ctas": int(len(cta_first) - 1),
+                     "partial_blocks": n_parts},
+            "call_roofline": {"t_roof_us": t_call_roof * 1e6,
+                              "frac": t_call_roof / (value_us * 1e-6),
+                              "bytes": work["call_bytes"], "flops": work["flops"]},
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": launches_per_call * steps, "clocks": clocks,
+        }
+        del q, k, v, t, out, lse
+        torch.cuda.empty_cache()
+        return entry
+
+
+PER_CONFIG_ORDER = ["decode", "tiny", "batching", "wide", "prefill"]
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", default="decode", choices=sorted(WORKLOADS))
+    ap.add_argument("--config", default="decode", choices=sorted(WORKLOADS),
+                    help="the workload of the line's top-level value")
+    ap.add_argument("--per-config", default="all",
+                    help="comma-separated workloads measured into per_config ('all', 'none')")
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -287,173 +506,48 @@ def main():
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     build.build()
     binding.load()
+    bench = Bench(torch, binding, local, world, dist)
 
-    w = draw(WORKLOADS[args.config])
-    s = w.spec
-    table = binding.fork(w.prefix_pages, w.suffix_lens, s.page_size, w.free_pages,
-                         w.max_pages_per_branch)
-
-    def host_bf16(bits):
-        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
-
-    h_q, h_k, h_v = host_bf16(w.q), host_bf16(w.k_pool), host_bf16(w.v_pool)
-    h_t = torch.from_numpy(table)
-    q, k, v, t = (x.cuda() for x in (h_q, h_k, h_v, h_t))
-    R = w.total_rows
-    out = torch.empty((R, s.h_q, s.d), dtype=torch.float32, device="cuda")
-    lse = torch.empty((R, s.h_q), dtype=torch.float32, device="cuda")
-    l2 = torch.cuda.get_device_properties(local).L2_cache_size
-    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device="cuda")
-    flush_rd = torch.ones(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device="cuda")
-
-    def flush_l2():
-        # Write a buffer twice the L2 size, then read another one: the timed call
-        # starts with none of its inputs in L2 and no dirty lines left to write back.
-        flush.zero_()
-        flush_rd.sum()
-
-    def call():
-        binding.attn(q, k, v, t, s.prefix_len, w.suffix_lens, w.q_rows, s.h_q, s.h_kv,
-                     s.page_size, s.scale, s.causal, out=out, lse=lse)
-
-    for _ in range(max(3, args.warmup)):
-        flush_l2()
-        call()
-    torch.cuda.synchronize()
-    rc = binding.last_error()
-    if rc != binding.OK:
-        raise RuntimeError(f"device error {binding.strerror(rc)}")
-    units, cta_first, n_parts = binding.plan(
-        w.suffix_lens, w.q_rows, s.prefix_len, s.h_q, s.h_kv, s.page_size, s.causal,
-        torch.cuda.get_device_properties(local).multi_processor_count)
-    launches_per_call = 1 + (1 if n_parts > 0 else 0)
-
-    sampler = ClockSampler(gpu_id_for_smi(torch, local))
-    t_end = time.perf_counter() + args.soak_s
-    while time.perf_counter() < t_end:   # untimed soak: clocks settle and get sampled
-        flush_l2()
-        call()
-        torch.cuda.synchronize()
-    stream = torch.cuda.current_stream()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
-    for quad in ev:              # the raw CUDA events are created at first record
-        for e in quad:
-            e.record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    for e0, e1, _, _ in ev:
-        flush_l2()                         # L2 flushed between timed calls
-        e0.record(stream)
-        call()
-        e1.record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    clocks = sampler.stop()
-    # The attention kernel alone, in a second pass: events recorded between it
-    # and a separate merge launch would stop the merge from overlapping it, so
-    # they stay out of the pass the call time comes from.
-    for _, _, k0, k1 in ev:
-        flush_l2()
-        binding.set_profile_events(k0, k1)  # brackets the split-KV kernel alone
-        call()
-    torch.cuda.synchronize()
-    binding.set_profile_events(None, None)
-    call_ms = np.array([a.elapsed_time(b) for a, b, _, _ in ev])
-    split_ms = np.array([a.elapsed_time(b) for _, _, a, b in ev])
-    rc = binding.last_error()
-    if rc != binding.OK:
-        raise RuntimeError(f"device error {binding.strerror(rc)}")
-    mean_call = float(call_ms.mean())
-    mean_split = float(split_ms.mean())
-    mean_call, mean_split = max_over_ranks([mean_call, mean_split], dist if world > 1 else None,
-                                           "cuda")
-
-    # end to end: inputs from pinned host memory, result read back, every step
-    e2e = None
-    if not args.no_e2e:
-        p_q, p_k, p_v, p_t = (x.pin_memory() for x in (h_q, h_k, h_v, h_t))
-        p_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        p_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-        n_e2e = max(3, min(args.steps, 20))
-        e2e_ms = []
-        for i in range(n_e2e + 2):
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            flush_l2()
-            a.record(stream)
-            q.copy_(p_q, non_blocking=True)
-            k.copy_(p_k, non_blocking=True)
-            v.copy_(p_v, non_blocking=True)
-            t.copy_(p_t, non_blocking=True)
-            call()
-            p_out.copy_(out, non_blocking=True)
-            p_lse.copy_(lse, non_blocking=True)
-            b.record(stream)
-            torch.cuda.synchronize()
-            if i >= 2:
-                e2e_ms.append(a.elapsed_time(b))
-        e2e_val = float(np.mean(e2e_ms)) * 1e3
-        e2e_val = max_over_ranks([e2e_val], dist if world > 1 else None, "cuda")[0]
-        h2d = sum(x.numel() * x.element_size() for x in (p_q, p_k, p_v, p_t))
-        d2h = sum(x.numel() * x.element_size() for x in (p_out, p_lse))
-        e2e = {"value": e2e_val, "unit": "us/call", "h2d_bytes_per_step": int(h2d),
-               "d2h_bytes_per_step": int(d2h),
-               "note": "q, K/V page pool and page table copied from pinned host memory, "
-                       "out and lse copied back, every step"}
-
-    work = algorithmic_work(w)
-    peaks = load_peaks()
-    t_split = mean_split * 1e-3
-    t_hbm = work["split_bytes"] / (peaks["hbm"] * 1e9)
-    t_tc = work["flops"] / (peaks["tc"] * 1e12)
-    if t_hbm >= t_tc:
-        achieved = work["split_bytes"] / t_split / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm"], "unit": "GB/s"}
-    else:
-        achieved = work["flops"] / t_split / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["tc"], "unit": "TFLOP/s"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = ncu_traffic(args.config)
-    roof["kernel"] = "attn_fwd_kernel"
-    roof["peak_source"] = f"{peaks['source']} (MEASURED_PEAKS.json burst figure)" \
-        if peaks["source"] == "measured" else "fallback"
-    t_call_roof = max(work["call_bytes"] / (peaks["hbm"] * 1e9), t_tc)
-    value_us = mean_call * 1e3
-
-    cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
-        us, dt, nrows, threads, reps = oracle_sample(w, budget_s=15.0)
-        cpu = {"value": us, "unit": "us/call", "cores": threads, "kind": "oracle",
-               "sample": f"{nrows} of {R} query tokens (all {s.h_q} heads) x {reps} "
-                         f"repetitions, {dt:.1f} s, extrapolated to the full call by "
-                         f"visible keys"}
+    names = parse_per_config(args.per_config)
+    e2e_steps = 0 if args.no_e2e else max(3, min(args.steps, 20))
+    head = bench.run(args.config, args.steps, args.warmup, args.soak_s, e2e_steps,
+                     0.0 if args.no_cpu_baseline else 15.0)
+    per = {args.config: head} if args.config in names else {}
+    for name in names:
+        if name == args.config:
+            continue
+        per[name] = bench.run(name, args.steps, args.warmup, min(args.soak_s, 0.5),
+                              0 if args.no_e2e else max(3, min(args.steps, 10)),
+                              0.0 if args.no_cpu_baseline else 6.0)
 
     line = {
-        "metric": METRIC, "value": value_us, "unit": "us/call", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_call,
+        "metric": METRIC, "value": head["value"], "unit": "us/call", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["value"] / 1e3,
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": args.config, "h_q": s.h_q, "h_kv": s.h_kv, "d": s.d,
-                   "branches": w.num_branches, "q_rows": int(R), "prefix_len": s.prefix_len,
-                   "suffix_tokens": int(w.suffix_lens.sum()), "page_size": s.page_size,
-                   "causal": s.causal, "work_units": int(len(units)),
-                   "persistent_ctas": int(len(cta_first) - 1), "partial_blocks": n_parts,
-                   "l2": "flushed between timed calls (write 2x L2, then read 2x L2)",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "call_roofline": {"t_roof_us": t_call_roof * 1e6, "frac": t_call_roof / (value_us * 1e-6),
-                          "bytes": work["call_bytes"], "flops": work["flops"]},
-        "split_kernel_us": mean_split * 1e3,
-        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": launches_per_call * args.steps, "clocks": clocks,
+        "config": head["config"], "plan": head["plan"],
+        "call_roofline": head["call_roofline"],
+        "split_kernel_us": head["kernel_us"],
+        "roofline": head["roofline"], "cpu_baseline": head["cpu_baseline"], "e2e": head["e2e"],
+        "gpu_launches": head["gpu_launches"], "clocks": head["clocks"],
+        "per_config": {n: per[n] for n in PER_CONFIG_ORDER if n in per},
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def parse_per_config(spec: str):
+    if spec == "all":
+        return list(PER_CONFIG_ORDER)
+    if spec in ("", "none"):
+        return []
+    names = [x.strip() for x in spec.split(",") if x.strip()]
+    for n in names:
+        if n not in WORKLOADS:
+            raise SystemExit(f"unknown workload {n!r}")
+    return names
 
 
 if __name__ == "__main__":

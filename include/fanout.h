@@ -320,6 +320,9 @@ FANOUT_API int fanout_selftest_wait_timeout(int64_t limit_ns, fanout_stream_t st
  *   - the first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
  *     before any stream capture;
+ *   - FANOUT_EUNSUPPORTED, with nothing done, when `stream` is capturing: each
+ *     call copies its plan into the array from host memory that lives only
+ *     for the call;
  *   - all calls share the one array, and it keeps the last call's contents.
  *     Nothing in it needs clearing (each call writes all it reads), but calls
  *     that overlap on the GPU (two streams, or a new call before the previous

@@ -51,6 +51,9 @@
 // returns.
 #include <cuda_bf16.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "fanout_internal.h"
 #include "merge_row.cuh"
 #include "ptx_sm100.cuh"
@@ -1087,15 +1090,23 @@ __global__ void __launch_bounds__(Cfg<NQ>::kThreads, 1) __maxnreg__(NQ == 2 ? 20
 template <int NQ>
 cudaError_t launch_nq(const SplitParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                       const CUtensorMap& tm_v, int grid, bool cooperative, cudaStream_t stream) {
-    static bool attr_set[64] = {};  // the attribute is set once per device
+    // The shared-memory attribute is set once per device (under a lock: calls
+    // on several host threads may arrive here together).
+    static std::atomic<bool> attr_set[64];
+    static std::mutex attr_mu;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-        e = cudaFuncSetAttribute(attn_fwd_kernel<NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 Cfg<NQ>::kSmemAlloc);
-        if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 64) attr_set[dev] = true;
+    const bool known = dev >= 0 && dev < 64;
+    if (!known || !attr_set[dev].load(std::memory_order_acquire)) {
+        std::lock_guard<std::mutex> lk(attr_mu);
+        if (!known || !attr_set[dev].load(std::memory_order_relaxed)) {
+            e = cudaFuncSetAttribute(attn_fwd_kernel<NQ>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     Cfg<NQ>::kSmemAlloc);
+            if (e != cudaSuccess) return e;
+            if (known) attr_set[dev].store(true, std::memory_order_release);
+        }
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);

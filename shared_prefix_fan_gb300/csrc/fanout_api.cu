@@ -15,7 +15,7 @@
 #include <vector>
 
 #include "../../include/fanout.h"
-#include "fanout_internal.h"
+#include "plan.h"
 
 using namespace fanout;
 
@@ -30,7 +30,11 @@ unsigned long long g_wait_limit_ns = 1000000000ull;
 cudaEvent_t g_ev_before = nullptr;
 cudaEvent_t g_ev_after = nullptr;
 
+// One per (device, stream). Its mutex serialises the calls on that stream's
+// workspace (plan cache, buffer, upload, launch); calls on other streams only
+// share g_mu for the map lookup and the option reads.
 struct Workspace {
+    std::mutex mu;
     void* buf = nullptr;
     size_t cap = 0;
     std::vector<int32_t> key;  // plan cache key
@@ -248,8 +252,7 @@ int fanout_set_option(int32_t option, int64_t value) {
     switch (option) {
         case FANOUT_OPT_SPLITS:
             if (value < 0) return FANOUT_EINVAL;
-            g_force_splits = value;
-            for (auto& kv : g_ws) kv.second->plan_ready = false;
+            g_force_splits = value;  // part of every plan key: cached plans are not reused
             return FANOUT_OK;
         case FANOUT_OPT_VALIDATE_TABLE: g_validate_table = value; return FANOUT_OK;
         case FANOUT_OPT_WAIT_LIMIT_NS:
@@ -258,8 +261,7 @@ int fanout_set_option(int32_t option, int64_t value) {
             return FANOUT_OK;
         case FANOUT_OPT_NUM_SMS:
             if (value < 0) return FANOUT_EINVAL;
-            g_num_sms_override = value;
-            for (auto& kv : g_ws) kv.second->plan_ready = false;
+            g_num_sms_override = value;  // part of every plan key as well
             return FANOUT_OK;
         case FANOUT_OPT_FUSED_MERGE:
             if (value != 0 && value != 1) return FANOUT_EINVAL;
@@ -288,8 +290,7 @@ int fanout_plan(const int32_t* suffix_lens, const int32_t* q_rows_per_branch,
     if (cap < 0 || (cap > 0 && !units) || cta_cap < 0 || (cta_cap > 0 && !cta_first))
         return FANOUT_EINVAL;
     PlanInput in{suffix_lens, q_rows_per_branch, num_branches, prefix_len, H_q, H_kv,
-                 page_size, causal, num_sms > 0 ? num_sms : 148,
-                 static_cast<int32_t>(g_force_splits)};
+                 page_size, causal, num_sms > 0 ? num_sms : 148, current_force_splits()};
     Plan plan;
     st = build_plan(in, plan);
     if (st != FANOUT_OK) return st;
@@ -318,10 +319,11 @@ int fanout_plan_step(const int32_t* prev_suffix_lens, const int32_t* suffix_lens
     if (cap < 0 || (cap > 0 && !units) || cta_cap < 0 || (cta_cap > 0 && !cta_first))
         return FANOUT_EINVAL;
     const int32_t sms = num_sms > 0 ? num_sms : 148;
+    const int32_t splits = current_force_splits();
     PlanInput prev{prev_suffix_lens, q_rows_per_branch, num_branches, prefix_len, H_q, H_kv,
-                   page_size, causal, sms, static_cast<int32_t>(g_force_splits)};
+                   page_size, causal, sms, splits};
     PlanInput in{suffix_lens, q_rows_per_branch, num_branches, prefix_len, H_q, H_kv,
-                 page_size, causal, sms, static_cast<int32_t>(g_force_splits)};
+                 page_size, causal, sms, splits};
     Plan plan;
     if ((st = build_plan(prev, plan)) != FANOUT_OK) return st;
     const bool kept = patch_plan(in, plan);
@@ -357,12 +359,34 @@ int fanout_attn(const void* q, const void* k_pages, const void* v_pages,
     if (st != FANOUT_OK) return st;
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
 
-    std::lock_guard<std::mutex> lk(g_mu);
     int dev = 0;
     cudaError_t ce = cudaGetDevice(&dev);
     if (ce != cudaSuccess) return status_from_cuda(ce);
 
-    if (g_validate_table) {
+    // Options and the workspace under the process-wide lock; everything after
+    // under the workspace's own lock only.
+    int64_t validate_table, fused_merge;
+    int32_t splits;
+    unsigned long long wait_limit_ns;
+    cudaEvent_t ev_before, ev_after;
+    int sms;
+    Workspace* ws;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        validate_table = g_validate_table;
+        fused_merge = g_fused_merge;
+        splits = static_cast<int32_t>(g_force_splits);
+        wait_limit_ns = g_wait_limit_ns;
+        ev_before = g_ev_before;
+        ev_after = g_ev_after;
+        sms = device_sms(dev);
+        Workspace*& slot = g_ws[{dev, stream}];
+        if (!slot) slot = new Workspace();
+        ws = slot;
+    }
+    std::lock_guard<std::mutex> wlk(ws->mu);
+
+    if (validate_table) {
         std::vector<int32_t> tab(static_cast<size_t>(num_branches) * max_pages_per_branch);
         ce = cudaMemcpyAsync(tab.data(), page_table, tab.size() * sizeof(int32_t),
                              cudaMemcpyDeviceToHost, stream);
@@ -379,24 +403,21 @@ int fanout_attn(const void* q, const void* k_pages, const void* v_pages,
         }
     }
 
-    const int sms = device_sms(dev);
-    Workspace*& ws = g_ws[{dev, stream}];
-    if (!ws) ws = new Workspace();
     std::vector<int32_t> key = {prefix_len, num_branches, H_q, H_kv, page_size, causal, sms,
-                                static_cast<int32_t>(g_force_splits)};
+                                splits};
     key.insert(key.end(), suffix_lens, suffix_lens + num_branches);
     key.insert(key.end(), q_rows_per_branch, q_rows_per_branch + num_branches);
     // A call that differs from the cached plan's only in suffix lengths (a
     // decode step) keeps the plan when every key range keeps its tile count:
     // only the unit table moves (new range ends and causal positions).
     const size_t fixed = 8;  // key entries before the suffix lengths
+    const PlanInput in{suffix_lens, q_rows_per_branch, num_branches, prefix_len, H_q, H_kv,
+                       page_size, causal, sms, splits};
     bool patched = false;
     if (ws->plan_ready && key != ws->key && key.size() == ws->key.size() &&
         std::equal(key.begin(), key.begin() + fixed, ws->key.begin()) &&
         std::equal(key.begin() + fixed + num_branches, key.end(),
                    ws->key.begin() + fixed + num_branches)) {
-        PlanInput in{suffix_lens, q_rows_per_branch, num_branches, prefix_len, H_q, H_kv,
-                     page_size, causal, sms, static_cast<int32_t>(g_force_splits)};
         if (patch_plan(in, ws->plan)) {
             ce = cudaMemcpyAsync(static_cast<uint8_t*>(ws->buf) + ws->layout.units,
                                  ws->plan.units.data(), ws->plan.units.size() * sizeof(Unit),
@@ -410,8 +431,6 @@ int fanout_attn(const void* q, const void* k_pages, const void* v_pages,
         }
     }
     if (!patched && (!ws->plan_ready || key != ws->key)) {
-        PlanInput in{suffix_lens, q_rows_per_branch, num_branches, prefix_len, H_q, H_kv,
-                     page_size, causal, sms, static_cast<int32_t>(g_force_splits)};
         ws->plan_ready = false;
         if ((st = build_plan(in, ws->plan)) != FANOUT_OK) return st;
         ws->layout = plan_layout(ws->plan);
@@ -440,10 +459,10 @@ int fanout_attn(const void* q, const void* k_pages, const void* v_pages,
     }
     if (++ws->epoch == 0) ws->epoch = 1;  // 0 is the flags' initial value
     CallArgs a{q, k_pages, v_pages, page_table, max_pages_per_branch, num_pages, H_q, H_kv,
-               page_size, out_dtype == FANOUT_OUT_BF16, scale, out, lse, R, g_wait_limit_ns,
-               static_cast<int32_t>(g_fused_merge), ws->epoch};
+               page_size, out_dtype == FANOUT_OUT_BF16, scale, out, lse, R, wait_limit_ns,
+               static_cast<int32_t>(fused_merge), ws->epoch};
     return launch_plan(a, ws->plan, ws->layout, static_cast<uint8_t*>(ws->buf), stream,
-                       g_ev_before, g_ev_after);
+                       ev_before, ev_after);
 }
 
 int fanout_lse_merge(const float* part_o, const float* part_ml, int32_t n_parts, int64_t n_out,
@@ -511,15 +530,21 @@ int fanout_release(void) {
     std::lock_guard<std::mutex> lk(g_mu);
     int cur = 0;
     cudaGetDevice(&cur);
+    // The workspace records stay (a call on another thread may hold one between
+    // the map lookup and its own lock); only their device buffers and plans go.
     for (auto& kv : g_ws) {
-        if (kv.second->buf) {
+        Workspace* ws = kv.second;
+        std::lock_guard<std::mutex> wlk(ws->mu);
+        if (ws->buf) {
             cudaSetDevice(kv.first.first);
             cudaDeviceSynchronize();
-            cudaFree(kv.second->buf);
+            cudaFree(ws->buf);
         }
-        delete kv.second;
+        ws->buf = nullptr;
+        ws->cap = 0;
+        ws->plan_ready = false;
+        ws->key.clear();
     }
-    g_ws.clear();
     cudaSetDevice(cur);
     return FANOUT_OK;
 }

@@ -18,7 +18,9 @@
 // The host-side name of the array is only a stand-in, not a device address;
 // the address is looked up with cudaGetSymbolAddress once per device, by the
 // first call on that device (so make that first call before any stream
-// capture). All calls share the array and it keeps the last call's contents:
+// capture). A call on a stream that is capturing is refused
+// (FANOUT_EUNSUPPORTED, nothing done): the plan is copied from host memory
+// that lives only for the call. All calls share the array and it keeps the last call's contents:
 // nothing in it is read before the same call writes it (the plan is uploaded
 // every call, and every partial slot the merge reads is written by one unit
 // of the same call) except the fused merge's per-CTA flags at its start,
@@ -34,7 +36,7 @@
 #include <vector>
 
 #include "../../include/fanout.h"
-#include "fanout_internal.h"
+#include "plan.h"
 
 using namespace fanout;
 
@@ -91,6 +93,12 @@ extern "C" FANOUT_API int fanout_attn_noalloc(
     st = validate_call(q, k_pages, v_pages, page_table, suffix_lens, num_branches, prefix_len,
                        max_pages_per_branch, num_pages, page_size, scale, out_dtype, out);
     if (st != FANOUT_OK) return st;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    // The plan is copied to the array from host memory that lives only for this
+    // call; a captured copy would read it after it is gone. Refused, nothing done.
+    cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &capture) != cudaSuccess) return FANOUT_ECUDA;
+    if (capture != cudaStreamCaptureStatusNone) return FANOUT_EUNSUPPORTED;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return FANOUT_ECUDA;
     int sms = 0;
@@ -146,7 +154,6 @@ extern "C" FANOUT_API int fanout_attn_noalloc(
 
     uint8_t* scratch = nullptr;
     if ((st = scratch_for_device(dev, &scratch)) != FANOUT_OK) return st;
-    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     if (upload_plan(plan, L, scratch, stream) != cudaSuccess) return FANOUT_ECUDA;
     uint32_t epoch;
     {

@@ -5,6 +5,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "fanout_internal.h"
@@ -87,16 +88,22 @@ cudaError_t launch_lse_merge(const MergeParams& p, cudaStream_t stream) {
 // only a stand-in; the address must come from the runtime, per device).
 // Looked up once per device (with that device current) and cached.
 cudaError_t err_word_ptr(int32_t** ptr) {
-    static int32_t* cached[64] = {};
+    static std::atomic<int32_t*> cached[64];  // filled once per device, read lock-free
+    static std::mutex mu;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64 && cached[dev]) {
-        *ptr = cached[dev];
-        return cudaSuccess;
+    const bool known = dev >= 0 && dev < 64;
+    if (known) {
+        int32_t* c = cached[dev].load(std::memory_order_acquire);
+        if (c) {
+            *ptr = c;
+            return cudaSuccess;
+        }
     }
+    std::lock_guard<std::mutex> lk(mu);
     e = cudaGetSymbolAddress(reinterpret_cast<void**>(ptr), g_err_word);
-    if (e == cudaSuccess && dev >= 0 && dev < 64) cached[dev] = *ptr;
+    if (e == cudaSuccess && known) cached[dev].store(*ptr, std::memory_order_release);
     return e;
 }
 

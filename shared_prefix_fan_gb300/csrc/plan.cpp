@@ -35,7 +35,7 @@
 #include <tuple>
 #include <vector>
 
-#include "fanout_internal.h"
+#include "plan.h"
 
 namespace fanout {
 namespace {

@@ -10,7 +10,7 @@
 #include <mutex>
 
 #include "../../include/fanout.h"
-#include "fanout_internal.h"
+#include "plan.h"
 
 namespace fanout {
 namespace {

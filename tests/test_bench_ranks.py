@@ -60,9 +60,17 @@ def test_reference_arm_prints_from_rank_zero_only():
     env["RANK"] = "0"
     env["LOCAL_RANK"] = "0"
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
-                        "--config", "tiny", "--steps", "1", "--warmup", "0"],
+                        "--config", "tiny", "--steps", "1", "--warmup", "0",
+                        "--per-config", "tiny,batching"],
                        capture_output=True, text=True, env=env, timeout=300)
     assert r.returncode == 0
     line = json.loads(r.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["unit"] == "us/call"
     assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
+    # the same workload description as the GPU arm's line, and one entry per
+    # requested workload
+    import bench
+    from shared_prefix_fan_gb300.workloads import WORKLOADS, draw
+    assert line["config"] == bench.workload_config(draw(WORKLOADS["tiny"]), 2)
+    assert list(line["per_config"]) == ["tiny", "batching"]
+    assert line["per_config"]["batching"]["cpu_baseline"]["value"] > 0

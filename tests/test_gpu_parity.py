@@ -29,10 +29,34 @@ def test_full_workload(name):
     compare(out, lse, *oracle_ref(w), what=name)
 
 
-@pytest.mark.parametrize("name,every", [("wide", 16), ("prefill", 512)])
+def partial_unit_tokens(w):
+    """Tokens of every unit of the plan the call runs that writes a partial
+    (merged later), and the units themselves, planned for this device."""
+    s = w.spec
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    units, _, _ = binding.plan(w.suffix_lens, w.q_rows, s.prefix_len, s.h_q, s.h_kv,
+                               s.page_size, s.causal, sms)
+    parts = units[units[:, 7] >= 0]
+    toks = set()
+    for u in parts:
+        toks.update(range(int(u[2]), int(u[2] + u[3])))
+    return parts, toks
+
+
+@pytest.mark.parametrize("name,every", [("wide", 16), ("prefill", 64)])
 def test_large_workload_sampled(name, every):
+    """Full-size workloads on sampled tokens: every `every`-th token, each
+    branch's first and last, and -- where only some tokens have partials (the
+    long prefill's tail cuts, merged through the sparse key list) -- every
+    token of every partial unit, so each merge path the plan takes is checked."""
     w = draw(WORKLOADS[name])
-    rows = sample_rows(w, every)
+    rows = set(sample_rows(w, every).tolist())
+    parts, part_toks = partial_unit_tokens(w)
+    if len(part_toks) < w.total_rows:   # a sparse merge: cover all of it
+        rows |= part_toks
+    rows = np.array(sorted(rows), dtype=np.int32)
+    for u in parts:   # every partial unit has sampled tokens
+        assert ((rows >= u[2]) & (rows < u[2] + u[3])).any(), u
     out, lse = DevWorkload(w).run()
     ref_o, ref_l = oracle_ref(w, rows=rows)
     compare(out, lse, ref_o, ref_l, rows=rows, what=name)

@@ -210,3 +210,35 @@ def test_plan_step_random(seed):
     else:
         fresh, fresh_cta, _ = binding.plan(S1, T, P, hq, hkv, ps, causal, sms)
         assert (units == fresh).all() and (cta == fresh_cta).all()
+
+
+def test_planning_from_two_threads_at_once():
+    """Two host threads plan (and set options) concurrently through the C ABI:
+    each gets exactly the plan a lone call gives (ctypes releases the GIL for
+    the duration of each call, so the library's planning really overlaps)."""
+    import threading
+
+    cases = []
+    for name in ("decode", "batching", "wide"):
+        w = draw(WORKLOADS[name])
+        s = w.spec
+        args = (w.suffix_lens, w.q_rows, s.prefix_len, s.h_q, s.h_kv, s.page_size, s.causal, 152)
+        cases.append((args, binding.plan(*args)))
+    errors = []
+
+    def worker(k):
+        try:
+            for i in range(8):
+                args, (units, cta, n_parts) = cases[(k + i) % len(cases)]
+                binding.set_option(binding.OPT_VALIDATE_TABLE, 0)
+                got_u, got_c, got_n = binding.plan(*args)
+                assert (got_u == units).all() and (got_c == cta).all() and got_n == n_parts
+        except Exception as e:  # noqa: BLE001 -- reported by the main thread
+            errors.append(repr(e))
+
+    threads = [threading.Thread(target=worker, args=(k,)) for k in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors

@@ -3,9 +3,11 @@ device memory during a call (an engine that owns all device memory through its
 own pool, code that cannot afford cudaFree's device-wide synchronisation, or
 code running where allocation is not allowed). It keeps its work plan and
 split partials in the library's fixed scratch array instead of a cudaMalloc'd
-workspace. Checked against fanout_attn, through the C ABI, on two calls in a
-row with different problems (the shared array keeps the previous call's
-contents), and for the clear rejection of a problem too big for the array.
+workspace. Checked against fanout_attn and the fp64 oracle, through the C ABI,
+on two calls in a row with different problems (the shared array keeps the
+previous call's contents), on consecutive decode steps, for the clear
+rejection of a problem too big for the array, and for the refusal of a stream
+that is being captured.
 
 This file is collected last on purpose (pytest orders files by name)."""
 import numpy as np
@@ -33,6 +35,8 @@ def _close(a_out, a_lse, b_out, b_lse):
 
 
 def test_noalloc_matches_fanout_attn_on_two_calls():
+    from tests.gpu_helpers import compare, oracle_ref
+
     for name in ("decode", "batching"):   # two calls in a row, different plans
         dw = DevWorkload(draw(WORKLOADS[name]))
         ref_out, ref_lse = dw.run()
@@ -41,6 +45,34 @@ def test_noalloc_matches_fanout_attn_on_two_calls():
         assert _noalloc(dw, out, lse) == binding.OK
         assert binding.last_error() == binding.OK
         _close(out, lse, ref_out, ref_lse)
+        # and against the fp64 oracle, so a fault both entries share shows too
+        compare(out, lse, *oracle_ref(dw.w), what=f"no-alloc {name}")
+
+
+def test_noalloc_refuses_a_capturing_stream():
+    """Each call copies its plan into the array from host memory that lives
+    only for the call, so a call on a stream being captured is refused with
+    nothing done (and the stream stays usable)."""
+    dw = DevWorkload(draw(WORKLOADS["tiny"]))
+    out = torch.zeros((dw.w.total_rows, dw.w.spec.h_q, 128), device="cuda")
+    lse = torch.zeros((dw.w.total_rows, dw.w.spec.h_q), device="cuda")
+    assert _noalloc(dw, out, lse) == binding.OK   # first call on the device: set-up
+    torch.cuda.synchronize()
+    out.zero_()
+    stream = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    s = dw.w.spec
+    with torch.cuda.stream(stream):
+        graph.capture_begin()
+        try:
+            rc = binding.attn_noalloc(dw.q, dw.k, dw.v, dw.table, s.prefix_len,
+                                      dw.w.suffix_lens, dw.w.q_rows, s.h_q, s.h_kv, s.page_size,
+                                      s.scale, s.causal, out, lse, stream=stream)
+        finally:
+            graph.capture_end()
+    assert rc == binding.EUNSUPPORTED
+    torch.cuda.synchronize()
+    assert (out == 0).all().item()
 
 
 def test_noalloc_rejects_problem_beyond_scratch():
@@ -71,19 +103,22 @@ def test_noalloc_long_prefill():
     _close(out, lse, ref_out, ref_lse)
 
 
-def test_noalloc_decode_steps():
+@pytest.mark.parametrize("q_rows", [[1, 1, 1, 1], [8, 8, 8]], ids=["one_token", "eight_tokens"])
+def test_noalloc_decode_steps(q_rows):
     """Decode steps through the no-allocation entry: it keeps the device's last
     plan while the suffix lengths move within their tiles (and plans anew when
-    a range gains a tile); every step matches the fp64 oracle."""
+    a range gains a tile); every step matches the fp64 oracle. With eight new
+    tokens per branch each suffix range ends at its last token's causal
+    position, which moves with every step."""
     import dataclasses
 
     import oracle
     from shared_prefix_fan_gb300.workloads import small_spec
     from tests.gpu_helpers import compare
 
-    S0 = np.array([100, 90, 110, 100], dtype=np.int32)
+    S0 = np.array([100, 90, 110, 100][:len(q_rows)], dtype=np.int32)
     grows = [0, 1, 2, 7, 40]
-    spec = small_spec(h_q=64, h_kv=8, page_size=64, prefix_len=2048, q_rows=[1, 1, 1, 1],
+    spec = small_spec(h_q=64, h_kv=8, page_size=64, prefix_len=2048, q_rows=q_rows,
                       suffix_lens=[int(x) for x in S0 + max(grows)], permute_prefix=True,
                       permute_suffix=True, seed=78)
     dw = DevWorkload(draw(spec))
