@@ -387,24 +387,25 @@ class Bench:
         if self.world > 1:
             self.dist.barrier()
         torch.cuda.synchronize()
-        for e0, e1, _, _ in ev:
+        # Each step times one call (e0..e1); after it, an untimed call with
+        # events around the attention kernel alone (k0..k1), so that both
+        # figures come from the same clock and power state (under a power cap
+        # the clocks drift within seconds). Events between the attention kernel
+        # and the merge launch would stop the merge from overlapping it, so they
+        # stay out of the timed calls.
+        for e0, e1, k0, k1 in ev:
             self.flush_l2()                    # L2 flushed between timed calls
             e0.record(stream)
             call()
             e1.record(stream)
+            self.flush_l2()
+            binding.set_profile_events(k0, k1)  # brackets the split-KV kernel alone
+            call()
+            binding.set_profile_events(None, None)
         torch.cuda.synchronize()
         if self.world > 1:
             self.dist.barrier()
         clocks = sampler.stop()
-        # The attention kernel alone, in a second pass: events recorded between it
-        # and a separate merge launch would stop the merge from overlapping it, so
-        # they stay out of the pass the call time comes from.
-        for _, _, k0, k1 in ev:
-            self.flush_l2()
-            binding.set_profile_events(k0, k1)  # brackets the split-KV kernel alone
-            call()
-        torch.cuda.synchronize()
-        binding.set_profile_events(None, None)
         call_ms = np.array([a.elapsed_time(b) for a, b, _, _ in ev])
         split_ms = np.array([a.elapsed_time(b) for _, _, a, b in ev])
         rc = binding.last_error()
@@ -466,7 +467,8 @@ class Bench:
                               "frac": t_call_roof / (value_us * 1e-6),
                               "bytes": work["call_bytes"], "flops": work["flops"]},
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": launches_per_call * steps, "clocks": clocks,
+            # the timed region holds each step's timed call and its kernel-only twin
+            "gpu_launches": 2 * launches_per_call * steps, "clocks": clocks,
         }
         del q, k, v, t, out, lse
         torch.cuda.empty_cache()

@@ -46,7 +46,8 @@
 // brings the next unit's Q into L2 one unit ahead; each softmax warp keeps its
 // unit's output fields in a shared-memory slot, and each group runs its
 // epilogue once dry before the first unit so that code is warm.
-// Every wait is bounded (mbar_wait); on expiry the CTA records
+// The producer signals the dependent merge launch once it has issued its last
+// copies. Every wait is bounded (mbar_wait); on expiry the CTA records
 // FANOUT_ETIMEOUT, drains its own in-flight copies and MMAs, frees TMEM and
 // returns.
 #include <cuda_bf16.h>
@@ -295,6 +296,13 @@ __device__ void producer_warp(const SplitParams& p, const Smem<NQ>& sm, const CU
         }
         ++k;
     }
+    // Every copy of this CTA is issued: the dependent merge grid may be
+    // scheduled now (once every CTA got here or exited), a few tiles before this
+    // CTA ends, so it is resident and has made its dry pass when the last CTA
+    // finishes. Signalling at the kernel's start instead kept merge blocks
+    // waiting beside the attention CTAs for the whole kernel, which measured
+    // 3-4 % slower on a long prefill (they take issue slots from the softmax).
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (!ok && lane == 0) {
         // Drain: every copy this warp started must land before the CTA exits.
         for (int s = 0; s < C::kStages; ++s)
@@ -1025,9 +1033,6 @@ __global__ void __launch_bounds__(Cfg<NQ>::kThreads, 1) __maxnreg__(NQ == 2 ? 20
     }
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // The dependent merge kernel may be scheduled now; it waits for this grid
-    // to complete before reading anything.
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
             ptx::mbar_init(sm.bar(C::BAR_FULL + s), 1);

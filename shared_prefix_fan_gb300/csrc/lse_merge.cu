@@ -19,29 +19,52 @@ __device__ int32_t g_err_word[4];
 
 namespace {
 
-// One warp per output row; kMergeBatch partials per pass: 24 for rows with
-// many partials (decode), 8 when every row has few. Blocks of two warps: small
-// enough to be resident beside an attention CTA (which leaves ~27 K registers
-// and 2 KB of shared memory of an SM free), so the grid starts, and runs its
-// dry pass, while the attention kernel is still working.
+// One warp per output row at a time; kMergeBatch partials per pass: 24 for
+// rows with many partials (decode), 8 when every row has few. Blocks of two
+// warps: small enough to be resident beside an attention CTA (which leaves
+// ~27 K registers and 2 KB of shared memory of an SM free), so part of the
+// grid starts, and runs its dry pass, while the attention kernel is still
+// working. The grid is at most what the device holds at once (the rest of it
+// starts the moment the attention CTAs leave, in one wave), and warps loop
+// over rows with the merge index read one row ahead, so after the wait a row
+// costs one memory round trip (its partials).
 constexpr int kMergeThreads = 64;
 template <int kMergeBatch>
 __global__ void __launch_bounds__(kMergeThreads, 1) lse_merge_kernel(const MergeParams p) {
     // Launched as a programmatic dependent of the attention kernel: this grid
     // is resident while that one runs. Before waiting for it to complete, each
-    // warp reads its first row's merge index and makes a dry run of the row
-    // (instruction and data caches warm, nothing written).
+    // warp reads the merge index of its first two rows and makes a dry run of
+    // the first (instruction and data caches warm, nothing written).
     const int lane = threadIdx.x & 31;
     const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
     const int64_t n0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    MergeIdx ix{0, 0, 0, make_int2(0, 0), 0};
-    if (n0 < p.n_out) {
-        ix = merge_index(p, n0, lane);
-        merge_row_ix<kMergeBatch>(p, ix, lane, true);
-    }
+    const MergeIdx none{0, 0, 0, make_int2(0, 0), 0};
+    MergeIdx cur = n0 < p.n_out ? merge_index(p, n0, lane) : none;
+    MergeIdx nxt = n0 + warps < p.n_out ? merge_index(p, n0 + warps, lane) : none;
+    if (n0 < p.n_out) merge_row_ix<kMergeBatch>(p, cur, lane, true);
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (n0 < p.n_out) merge_row_ix<kMergeBatch>(p, ix, lane);
-    for (int64_t n = n0 + warps; n < p.n_out; n += warps) merge_row<kMergeBatch>(p, n, lane);
+    for (int64_t n = n0; n < p.n_out; n += warps) {
+        const MergeIdx after = n + 2 * warps < p.n_out ? merge_index(p, n + 2 * warps, lane) : none;
+        merge_row_ix<kMergeBatch>(p, cur, lane);
+        cur = nxt;
+        nxt = after;
+    }
+}
+
+// Blocks of one merge kernel instance the device holds per SM (looked up once).
+template <int kMergeBatch>
+int merge_blocks_per_sm() {
+    static std::atomic<int> cached{0};
+    int v = cached.load(std::memory_order_relaxed);
+    if (v > 0) return v;
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, lse_merge_kernel<kMergeBatch>,
+                                                      kMergeThreads, 0) != cudaSuccess || occ <= 0) {
+        (void)cudaGetLastError();
+        occ = 8;
+    }
+    cached.store(occ, std::memory_order_relaxed);
+    return occ;
 }
 
 // One thread waits on a barrier that nothing will ever complete; the bounded
@@ -63,13 +86,15 @@ cudaError_t launch_lse_merge(const MergeParams& p, cudaStream_t stream) {
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int32_t most = p.merge_cnt ? p.merge_stride : p.n_parts;  // partials of the fullest row
+    const bool few = most <= 8;
     const int64_t rows_per_block = kMergeThreads / 32;
     const int64_t blocks_needed = (p.n_out + rows_per_block - 1) / rows_per_block;
-    const int grid =
-        static_cast<int>(std::min<int64_t>(blocks_needed, static_cast<int64_t>(sms) * 32));
+    const int per_sm = few ? merge_blocks_per_sm<8>() : merge_blocks_per_sm<24>();
+    const int grid = static_cast<int>(
+        std::min<int64_t>(blocks_needed, static_cast<int64_t>(sms) * per_sm));
     // Programmatic dependent launch: the merge grid may start while the
     // attention kernel finishes; griddepcontrol.wait orders the reads.
-    const int32_t most = p.merge_cnt ? p.merge_stride : p.n_parts;  // partials of the fullest row
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kMergeThreads);
@@ -80,7 +105,7 @@ cudaError_t launch_lse_merge(const MergeParams& p, cudaStream_t stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (most <= 8) return cudaLaunchKernelEx(&cfg, lse_merge_kernel<8>, p);
+    if (few) return cudaLaunchKernelEx(&cfg, lse_merge_kernel<8>, p);
     return cudaLaunchKernelEx(&cfg, lse_merge_kernel<24>, p);
 }
 
