@@ -307,7 +307,10 @@ def roofline_of(work, peaks, t_kernel_s, workload):
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm"], "unit": "GB/s"}
     else:
         achieved = work["flops"] / t_kernel_s / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["tc"], "unit": "TFLOP/s"}
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["tc"], "unit": "TFLOP/s",
+                # for a kernel that runs under the power cap (long prefill)
+                "peak_sustained": peaks["tc_sustained"],
+                "frac_sustained": achieved / peaks["tc_sustained"]}
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["traffic"] = ncu_traffic(workload)
     roof["algorithmic_bytes"] = work["split_bytes"]
