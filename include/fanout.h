@@ -265,7 +265,7 @@ FANOUT_API int fanout_set_option(int32_t option, int64_t value);
 FANOUT_API int fanout_set_profile_events(fanout_event_t before, fanout_event_t after);
 
 /* Host-side description of the work plan fanout_attn would run for a problem
- * (no device access), planned for `num_sms` persistent CTAs (<= 0: 148).
+ * (no device access), planned for `num_sms` persistent CTAs (<= 0: 152, a GB300's SM count).
  * Writes up to `cap` unit records of 8 int32 each, grouped by CTA:
  *   {kv_head, branch, tok_begin, n_tok, key_begin, key_end, pos_base, part}
  * (the query rows of n_tok tokens x the G heads of kv_head against keys

@@ -164,7 +164,7 @@ def kv_append(k_new, v_new, k_pages, v_pages, page_table, prefix_len: int, suffi
 
 
 def plan(suffix_lens, q_rows, prefix_len: int, h_q: int, h_kv: int, page_size: int,
-         causal: bool, num_sms: int = 148) -> Tuple[np.ndarray, np.ndarray, int]:
+         causal: bool, num_sms: int = 152) -> Tuple[np.ndarray, np.ndarray, int]:
     """The work plan fanout_attn would run: (units [n, 8], cta_first [n_cta+1], n_parts)."""
     sl, tq = _i32arr(suffix_lens), _i32arr(q_rows)
     lib = load()
@@ -182,7 +182,7 @@ def plan(suffix_lens, q_rows, prefix_len: int, h_q: int, h_kv: int, page_size: i
 
 
 def plan_step(prev_suffix_lens, suffix_lens, q_rows, prefix_len: int, h_q: int, h_kv: int,
-              page_size: int, causal: bool, num_sms: int = 148):
+              page_size: int, causal: bool, num_sms: int = 152):
     """The plan fanout_attn runs after a call that differed only in suffix
     lengths: (units [n, 8], cta_first [n_cta+1], n_parts, reused)."""
     ps_, sl, tq = _i32arr(prev_suffix_lens), _i32arr(suffix_lens), _i32arr(q_rows)

@@ -53,6 +53,9 @@ int status_from_cuda(cudaError_t e) {
 
 bool ok_align16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// The host-only planning calls' default CTA count: a GB300's SMs.
+constexpr int32_t kDefaultSms = 152;
+
 int device_sms(int dev) {
     if (g_num_sms_override > 0) return static_cast<int>(g_num_sms_override);
     int sms = 0;
@@ -75,7 +78,7 @@ int32_t current_fused_merge() {
 
 extern "C" {
 
-const char* fanout_version(void) { return "0.1.0"; }
+const char* fanout_version(void) { return "0.2.0"; }
 
 const char* fanout_strerror(int code) {
     switch (code) {
@@ -290,7 +293,7 @@ int fanout_plan(const int32_t* suffix_lens, const int32_t* q_rows_per_branch,
     if (cap < 0 || (cap > 0 && !units) || cta_cap < 0 || (cta_cap > 0 && !cta_first))
         return FANOUT_EINVAL;
     PlanInput in{suffix_lens, q_rows_per_branch, num_branches, prefix_len, H_q, H_kv,
-                 page_size, causal, num_sms > 0 ? num_sms : 148, current_force_splits()};
+                 page_size, causal, num_sms > 0 ? num_sms : kDefaultSms, current_force_splits()};
     Plan plan;
     st = build_plan(in, plan);
     if (st != FANOUT_OK) return st;
@@ -318,7 +321,7 @@ int fanout_plan_step(const int32_t* prev_suffix_lens, const int32_t* suffix_lens
     if (st != FANOUT_OK) return st;
     if (cap < 0 || (cap > 0 && !units) || cta_cap < 0 || (cta_cap > 0 && !cta_first))
         return FANOUT_EINVAL;
-    const int32_t sms = num_sms > 0 ? num_sms : 148;
+    const int32_t sms = num_sms > 0 ? num_sms : kDefaultSms;
     const int32_t splits = current_force_splits();
     PlanInput prev{prev_suffix_lens, q_rows_per_branch, num_branches, prefix_len, H_q, H_kv,
                    page_size, causal, sms, splits};

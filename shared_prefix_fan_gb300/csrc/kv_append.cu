@@ -95,7 +95,7 @@ cudaError_t launch_copy_pages(void* k_pool, void* v_pool, const int32_t* pairs, 
                               int32_t num_pages, int32_t* err, cudaStream_t stream) {
     const int64_t items = static_cast<int64_t>(n_pairs) * H_kv * rows;
     if (items <= 0) return cudaSuccess;
-    int dev = 0, sms = 148;
+    int dev = 0, sms = 152;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int64_t blocks = (items + 7) / 8;
@@ -111,7 +111,7 @@ cudaError_t launch_kv_append(const void* k_new, const void* v_new, void* k_pool,
                              cudaStream_t stream) {
     const int64_t items = static_cast<int64_t>(p.R) * p.H_kv;
     if (items <= 0) return cudaSuccess;
-    int dev = 0, sms = 148;
+    int dev = 0, sms = 152;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int64_t blocks = (items + 7) / 8;

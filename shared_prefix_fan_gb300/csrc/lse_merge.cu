@@ -83,7 +83,7 @@ __global__ void wait_selftest_kernel(int32_t* err, unsigned long long limit_ns) 
 
 cudaError_t launch_lse_merge(const MergeParams& p, cudaStream_t stream) {
     if (p.n_out <= 0) return cudaSuccess;
-    int dev = 0, sms = 148;
+    int dev = 0, sms = 152;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int32_t most = p.merge_cnt ? p.merge_stride : p.n_parts;  // partials of the fullest row

@@ -114,3 +114,39 @@ def test_bf16_output():
     ulp = np.abs(ref_bf) * 2.0 ** -8 + 1e-30
     assert (np.abs(o - ref_bf) <= ulp + 2e-3).all()
     compare(out, lse, ref_o, ref_l, what="bf16 out")
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_random_shapes(seed):
+    """Seeded random problems (branch count, new tokens and private suffix per
+    branch, prefix length, page size, GQA group, causal or not, page placement,
+    output dtype) through the C ABI against the fp64 oracle: planner paths the
+    fixed cases may not reach (ragged tails, a single branch, empty branches,
+    G from 1 to 16, one- and two-query-tile units)."""
+    rng = np.random.default_rng(9000 + seed)
+    B = int(rng.integers(1, 7))
+    ps = int(rng.choice([16, 32, 64, 128]))
+    P = ps * int(rng.integers(0, 24))
+    causal = bool(rng.integers(0, 2))
+    T = rng.integers(0, 40, size=B)
+    if T.sum() == 0:
+        T[0] = 1
+    S = T + rng.integers(0 if P else 1, 700, size=B)
+    h_kv = int(rng.choice([1, 2, 4, 8]))
+    G = int(rng.choice([1, 2, 4, 8, 16]))
+    spec = small_spec(h_q=h_kv * G, h_kv=h_kv, page_size=ps, prefix_len=P, causal=causal,
+                      q_rows=[int(x) for x in T], suffix_lens=[int(x) for x in S],
+                      permute_prefix=bool(rng.integers(0, 2)), permute_suffix=True,
+                      seed=9500 + seed)
+    w = draw(spec)
+    out_dtype = "bf16" if seed % 4 == 3 else "f32"
+    out, lse = DevWorkload(w).run(out_dtype=out_dtype)
+    ref_o, ref_l = oracle_ref(w)
+    if out_dtype == "bf16":
+        # a perfect kernel writes the oracle rounded to bf16 (half an ulp away)
+        ref_bf = torch.from_numpy(ref_o).float().to(torch.bfloat16).double().numpy()
+        o = out.double().cpu().numpy()
+        assert (np.abs(o - ref_bf) <= np.abs(ref_bf) * 2.0 ** -8 + 2e-3).all(), f"seed {seed}"
+        return
+    compare(out, lse, ref_o, ref_l, what=f"random {seed}: B={B} T={T.tolist()} "
+            f"S={S.tolist()} P={P} page={ps} G={G} H_kv={h_kv} causal={causal}")
