@@ -54,7 +54,7 @@ typedef struct CUevent_st *fanout_event_t;
 enum fanout_status {
     FANOUT_OK = 0,
     FANOUT_EINVAL = 1,        /* invalid argument (null pointer, bad size, bad page id) */
-    FANOUT_EUNSUPPORTED = 2,  /* valid problem outside what this build supports */
+    FANOUT_EUNSUPPORTED = 2,  /* valid problem outside what this library supports */
     FANOUT_ECUDA = 3,         /* a CUDA runtime/driver call failed */
     FANOUT_ENOMEM = 4,        /* workspace allocation failed */
     FANOUT_ETIMEOUT = 5       /* a bounded device-side wait ran out */
@@ -190,7 +190,7 @@ FANOUT_API int fanout_kv_append(const void *k_new, const void *v_new, void *k_pa
  *   q_rows_per_branch HOST int32 [num_branches] (>= 0); with causal != 0 each
  *                    must be <= suffix_lens[b].
  *   H_q, H_kv        H_q % H_kv == 0, G = H_q / H_kv <= 128.
- *   d                head dimension; this build supports d == 128.
+ *   d                head dimension; the library supports d == 128.
  *   page_size        one of 16, 32, 64, 128.
  *   scale            softmax scale applied to q.k, finite and > 0 (the pages
  *                    use 1/sqrt(d)).

@@ -84,7 +84,7 @@ const char* fanout_strerror(int code) {
     switch (code) {
         case FANOUT_OK: return "ok";
         case FANOUT_EINVAL: return "invalid argument";
-        case FANOUT_EUNSUPPORTED: return "unsupported problem for this build";
+        case FANOUT_EUNSUPPORTED: return "problem outside what this library supports";
         case FANOUT_ECUDA: return "CUDA error";
         case FANOUT_ENOMEM: return "out of device memory";
         case FANOUT_ETIMEOUT: return "device-side wait timed out";

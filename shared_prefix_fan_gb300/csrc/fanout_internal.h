@@ -11,7 +11,7 @@ namespace fanout {
 
 constexpr int kBM = 128;      // query rows per tile (tcgen05 M)
 constexpr int kBN = 128;      // keys per KV tile
-constexpr int kHD = 128;      // head dimension handled by this build
+constexpr int kHD = 128;      // the head dimension the kernels handle
 constexpr int kNoCausal = 1 << 30;  // pos_base for units that need no causal mask
 
 // One unit of split-KV work: the query rows of `n_tok` consecutive tokens
