@@ -340,7 +340,10 @@ FANOUT_API int fanout_attn_noalloc(const void *q, const void *k_pages, const voi
                 int32_t d, int32_t page_size, float scale, int32_t causal, void *out,
                 int32_t out_dtype, float *lse, fanout_stream_t stream);
 
-/* Frees the workspaces of every device and stream (synchronises first). */
+/* Frees the workspace buffers and cached plans of every device and stream
+ * (synchronising each device first); the next call on a stream allocates and
+ * plans again. Safe while other threads call fanout_attn: a call in flight
+ * finishes first (its workspace lock is taken before the buffer is freed). */
 FANOUT_API int fanout_release(void);
 
 /* Library version, "major.minor.patch". */

@@ -168,3 +168,35 @@ def test_empty_and_rowless_branches():
     w = draw(spec)
     out, lse = DevWorkload(w).run()
     compare(out, lse, *oracle_ref(w), what="row-less branches")
+
+
+def test_two_threads_on_two_streams():
+    """Two host threads call fanout_attn at the same time, each on its own
+    stream (so each uses its own workspace and plan cache, under its own lock):
+    every result equals the single-threaded result bit for bit."""
+    import threading
+
+    dws = [DevWorkload(draw(WORKLOADS["batching"])),
+           DevWorkload(draw(small_spec(h_q=16, h_kv=2, page_size=32, prefix_len=512,
+                                       q_rows=[5, 9, 3], suffix_lens=[70, 200, 33], seed=31)))]
+    refs = [dw.run() for dw in dws]
+    streams = [torch.cuda.Stream() for _ in dws]
+    results, errors = {}, []
+
+    def worker(k):
+        try:
+            with torch.cuda.stream(streams[k]):
+                for _ in range(6):
+                    results[k] = dws[k].run(stream=streams[k])
+        except Exception as e:  # noqa: BLE001 -- reported by the main thread
+            errors.append(repr(e))
+
+    threads = [threading.Thread(target=worker, args=(k,)) for k in range(len(dws))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    torch.cuda.synchronize()
+    assert not errors, errors
+    for k, (o, l) in enumerate(refs):
+        assert torch.equal(results[k][0], o) and torch.equal(results[k][1], l)
