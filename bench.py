@@ -339,6 +339,28 @@ class Bench:
         self.flush_w.zero_()
         self.flush_r.sum()
 
+    def read_floor_us(self, nbytes, steps):
+        """Mean time of one fanout_read_floor launch over `nbytes` of device
+        memory, L2 flushed before each and CUDA events around it: the shortest
+        time one kernel that reads those bytes takes here."""
+        torch, binding = self.torch, self.binding
+        stream = torch.cuda.current_stream()
+        buf = torch.zeros(nbytes // 16 * 16, dtype=torch.uint8, device="cuda")
+        xo = torch.zeros(1, dtype=torch.int32, device="cuda")
+        for _ in range(3):
+            self.flush_l2()
+            binding.read_floor(buf, xo)
+        ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(2)) for _ in range(steps)]
+        for a, b in ev:
+            self.flush_l2()
+            a.record(stream)
+            binding.read_floor(buf, xo)
+            b.record(stream)
+        torch.cuda.synchronize()
+        t = float(np.mean([a.elapsed_time(b) for a, b in ev])) * 1e3
+        del buf
+        return self.max_ranks([t])[0]
+
     def max_ranks(self, vals):
         return max_over_ranks(vals, self.dist if self.world > 1 else None, "cuda")
 
@@ -515,6 +537,12 @@ class Bench:
         work = algorithmic_work(w)
         peaks = load_peaks()
         roof = roofline_of(work, peaks, mean_split * 1e-3, name)
+        if roof["bound"] == "hbm":
+            # context for an HBM-bound kernel: a plain one-launch read of its
+            # algorithmic bytes, timed the same way (launch and ramp included)
+            floor = self.read_floor_us(work["split_bytes"], steps)
+            roof["read_floor_us"] = floor
+            roof["frac_of_read_floor"] = floor / (mean_split * 1e3)
         t_call_roof = max(work["call_bytes"] / (peaks["hbm"] * 1e9),
                           work["flops"] / (peaks["tc"] * 1e12))
         value_us = mean_call * 1e3

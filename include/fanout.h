@@ -303,6 +303,25 @@ FANOUT_API int fanout_plan_step(const int32_t *prev_suffix_lens, const int32_t *
 FANOUT_API int fanout_selftest_wait_timeout(int64_t limit_ns, fanout_stream_t stream);
 
 /*
+ * fanout_read_floor -- a calibration read; the pages have no counterpart.
+ * One launch streams `bytes` of device memory at `buf` once from HBM with
+ * plain 16-byte loads (four 512-thread CTAs per SM) and xors every 32-bit word
+ * of it into *xor_out. Timed like a fanout_attn call (after an L2 flush, CUDA
+ * events on `stream`), it is the shortest time one kernel that reads that many
+ * bytes takes on this device, launch and ramp included: the floor under an
+ * HBM-bound call, which a roofline at the steady copy bandwidth leaves out.
+ *   buf      dev, 16-byte aligned, read only.
+ *   bytes    > 0, a multiple of 16.
+ *   xor_out  dev uint32, 4-byte aligned, updated in place (*xor_out ^= xor of
+ *            the buffer's words); the caller sets it beforehand.
+ * FANOUT_EINVAL, with nothing launched, for a null pointer or a size or
+ * alignment outside these rules; FANOUT_ECUDA if the launch fails.
+ * Asynchronous on `stream`.
+ */
+FANOUT_API int fanout_read_floor(const void *buf, int64_t bytes, uint32_t *xor_out,
+                                 fanout_stream_t stream);
+
+/*
  * fanout_attn_noalloc -- fanout_attn that allocates no device memory.
  * The pages have no counterpart: this entry exists for callers of this
  * library that must not allocate device memory during a call -- a serving

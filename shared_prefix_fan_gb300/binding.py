@@ -49,6 +49,7 @@ ABI = {
                                         _i32, _i32p, _i32, _i32p, _i32p, _i32, _i32p, _i32p,
                                         _i32p]),
     "fanout_selftest_wait_timeout": (ctypes.c_int, [_i64, _vp]),
+    "fanout_read_floor": (ctypes.c_int, [_vp, _i64, _vp, _vp]),
     "fanout_release": (ctypes.c_int, []),
     "fanout_version": (ctypes.c_char_p, []),
 }
@@ -311,6 +312,19 @@ def set_profile_events(before=None, after=None) -> None:
 
 def selftest_wait_timeout(limit_ns: int = 20_000_000, stream=None) -> int:
     return int(load().fanout_selftest_wait_timeout(int(limit_ns), _stream_handle(stream)))
+
+
+def read_floor(buf, xor_out, stream=None) -> None:
+    """One plain streaming read of the device tensor `buf` (all its bytes);
+    *xor_out (a 1-element int32/uint32 CUDA tensor) ^= the xor of its words."""
+    import torch
+    if not buf.is_cuda or not buf.is_contiguous():
+        raise ValueError("buf must be a contiguous CUDA tensor")
+    if not xor_out.is_cuda or xor_out.dtype not in (torch.int32, torch.uint32):
+        raise ValueError("xor_out must be an int32 CUDA tensor")
+    _check(load().fanout_read_floor(buf.data_ptr(), int(buf.numel() * buf.element_size()),
+                                    xor_out.data_ptr(), _stream_handle(stream)),
+           "fanout_read_floor")
 
 
 def release() -> None:

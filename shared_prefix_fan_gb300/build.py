@@ -15,7 +15,7 @@ CSRC = os.path.join(HERE, "csrc")
 LIBDIR = os.path.join(HERE, "lib")
 LIB = os.path.join(LIBDIR, "libfanout.so")
 SOURCES = ["attn_fwd.cu", "lse_merge.cu", "kv_append.cu", "fanout_api.cu", "plan.cpp",
-           "runtime.cpp", "fanout_noalloc.cu"]
+           "runtime.cpp", "fanout_noalloc.cu", "read_floor.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler",
               "-fvisibility=hidden", "--expt-relaxed-constexpr"]

@@ -74,6 +74,9 @@ int32_t current_fused_merge() {
     std::lock_guard<std::mutex> lk(g_mu);
     return static_cast<int32_t>(g_fused_merge);
 }
+// read_floor.cu
+cudaError_t launch_stream_read(const void* buf, int64_t bytes, uint32_t* xor_out,
+                               cudaStream_t stream);
 }  // namespace fanout
 
 extern "C" {
@@ -527,6 +530,16 @@ int fanout_selftest_wait_timeout(int64_t limit_ns, fanout_stream_t stream) {
                               reinterpret_cast<cudaStream_t>(stream));
     if (ce != cudaSuccess) return status_from_cuda(ce);
     return fanout_last_error(stream);
+}
+
+int fanout_read_floor(const void* buf, int64_t bytes, uint32_t* xor_out,
+                      fanout_stream_t stream) {
+    if (buf == nullptr || xor_out == nullptr || bytes <= 0 || bytes % 16 != 0 ||
+        (reinterpret_cast<uintptr_t>(buf) & 15u) != 0 ||
+        (reinterpret_cast<uintptr_t>(xor_out) & 3u) != 0)
+        return FANOUT_EINVAL;
+    return status_from_cuda(
+        launch_stream_read(buf, bytes, xor_out, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int fanout_release(void) {

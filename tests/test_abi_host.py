@@ -49,6 +49,13 @@ def test_options_validated(lib):
     assert lib.fanout_set_option(binding.OPT_FUSED_MERGE, 1) == binding.OK
 
 
+def _device_visible() -> bool:
+    """These tests pass made-up addresses; a call that passes validation would
+    launch kernels on them, so such calls run only where no GPU is visible."""
+    import torch
+    return torch.cuda.is_available()
+
+
 def _attn_rc(lib, **kw):
     a = dict(q=1024, k=1024, v=1024, pt=1024, P=64, S=[32, 32], T=[2, 2], B=2, maxp=8,
              npages=16, hq=8, hkv=2, d=128, ps=16, scale=0.088, causal=1, out=1024, od=0,
@@ -67,7 +74,8 @@ def test_attn_rejects_bad_arguments_on_host(lib):
     E, U = binding.EINVAL, binding.EUNSUPPORTED
     assert _attn_rc(lib, d=64) == U
     assert _attn_rc(lib, ps=24) == U
-    assert _attn_rc(lib, P=40) not in (E, U)   # a prefix ending inside a page is accepted
+    if not _device_visible():   # accepted calls go on to launch: only with no GPU to launch on
+        assert _attn_rc(lib, P=40) not in (E, U)   # a prefix ending inside a page is accepted
     assert _attn_rc(lib, hq=6, hkv=4) == E     # H_q not a multiple of H_kv
     assert _attn_rc(lib, hq=256, hkv=1) == U   # G > 128
     assert _attn_rc(lib, T=[40, 2]) == E       # causal: more new tokens than suffix
@@ -92,3 +100,14 @@ def test_merge_rejects_bad_arguments_on_host(lib):
 
 def test_selftest_rejects_bad_limit(lib):
     assert lib.fanout_selftest_wait_timeout(0, None) == binding.EINVAL
+
+
+def test_read_floor_rejects_bad_arguments_on_host(lib):
+    E = binding.EINVAL
+    assert lib.fanout_read_floor(1032, 512, 2048, None) == E   # buffer not 16-byte aligned
+    assert lib.fanout_read_floor(1024, 520, 2048, None) == E   # size not a multiple of 16
+    assert lib.fanout_read_floor(1024, 0, 2048, None) == E
+    assert lib.fanout_read_floor(1024, -16, 2048, None) == E
+    assert lib.fanout_read_floor(None, 512, 2048, None) == E
+    assert lib.fanout_read_floor(1024, 512, None, None) == E
+    assert lib.fanout_read_floor(1024, 512, 2050, None) == E   # xor word not 4-byte aligned
