@@ -124,6 +124,19 @@ def workload_config(w, world: int) -> dict:
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
 
 
+def new_token_rows(w, table):
+    """(page ids, slots) of every query token's own K/V row, token-major: token
+    t of branch b sits at position prefix_len + S_b - T_b + t of the branch's
+    sequence, the row a decode step appends just before it attends."""
+    s = w.spec
+    T = np.asarray(w.q_rows, dtype=np.int64)
+    S = np.asarray(w.suffix_lens, dtype=np.int64)
+    br = np.repeat(np.arange(len(T)), T)
+    tok = np.arange(int(T.sum())) - np.repeat(np.cumsum(T) - T, T)
+    pos = s.prefix_len + S[br] - T[br] + tok
+    return table[br, pos // s.page_size], pos % s.page_size
+
+
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -474,11 +487,7 @@ class Bench:
             # result stay as above.
             T = np.asarray(w.q_rows, dtype=np.int64)
             S = np.asarray(w.suffix_lens, dtype=np.int64)
-            br = np.repeat(np.arange(len(T)), T)
-            tok = np.arange(int(T.sum())) - np.repeat(np.cumsum(T) - T, T)
-            pos = s.prefix_len + S[br] - T[br] + tok
-            pages = table[br, pos // s.page_size]
-            slot = pos % s.page_size
+            pages, slot = new_token_rows(w, table)
             k_rows = host_bf16(w.k_pool[pages, :, slot, :])   # [R, H_kv, d]
             v_rows = host_bf16(w.v_pool[pages, :, slot, :])
             # One staging buffer each way (one copy per direction per step):

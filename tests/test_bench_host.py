@@ -98,3 +98,31 @@ def test_traffic_is_reported_only_for_the_captured_kernel_source(tmp_path, monke
     assert bench.ncu_traffic("decode") == 123.0
     assert bench.ncu_traffic("wide") is None
     assert bench.ncu_traffic("prefill") is None
+
+
+@pytest.mark.parametrize("spec", [
+    WORKLOADS["tiny"],
+    small_spec(q_rows=[3, 0, 5, 1], suffix_lens=[20, 4, 33, 1], page_size=16, prefix_len=48,
+               permute_suffix=True, seed=11),
+], ids=["tiny", "ragged"])
+def test_new_token_rows_are_the_append_positions(spec):
+    """The resident-cache leg of the bench re-appends each query token's own
+    K/V row: the rows new_token_rows names must be exactly where the oracle's
+    append (before = S - T, add = T) writes them."""
+    w = draw(spec)
+    s = w.spec
+    table = oracle.fork(w.prefix_pages, w.suffix_lens, s.page_size, w.free_pages,
+                        w.max_pages_per_branch)
+    pages, slots = bench.new_token_rows(w, table)
+    R = w.total_rows
+    rng = np.random.default_rng(5)
+    k_new = rng.integers(1, 2**15, size=(R, s.h_kv, s.d), dtype=np.uint16)
+    v_new = rng.integers(1, 2**15, size=(R, s.h_kv, s.d), dtype=np.uint16)
+    T = np.asarray(w.q_rows, np.int32)
+    kp, vp = oracle.kv_append(k_new, v_new, w.k_pool, w.v_pool, table, s.prefix_len,
+                              np.asarray(w.suffix_lens, np.int32) - T, T)
+    assert np.array_equal(kp[pages, :, slots, :], k_new)
+    assert np.array_equal(vp[pages, :, slots, :], v_new)
+    kp[pages, :, slots, :] = w.k_pool[pages, :, slots, :]   # nothing else was written
+    vp[pages, :, slots, :] = w.v_pool[pages, :, slots, :]
+    assert np.array_equal(kp, w.k_pool) and np.array_equal(vp, w.v_pool)
