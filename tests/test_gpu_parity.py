@@ -150,3 +150,22 @@ def test_random_shapes(seed):
         return
     compare(out, lse, ref_o, ref_l, what=f"random {seed}: B={B} T={T.tolist()} "
             f"S={S.tolist()} P={P} page={ps} G={G} H_kv={h_kv} causal={causal}")
+
+
+@pytest.mark.parametrize("n_branches,prefix,page,h_q,h_kv,tmax,smax", [
+    (200, 2048, 16, 16, 2, 4, 200),
+    (1024, 512, 16, 8, 1, 1, 64),
+], ids=["200_branches", "1024_branches"])
+def test_many_branches(n_branches, prefix, page, h_q, h_kv, tmax, smax):
+    """Fan-out to many sub-agents (up to fanout_kv_append's 1024 branches):
+    hundreds of private suffix ranges per KV head, many units per CTA, a large
+    merge index; every row against the fp64 oracle."""
+    rng = np.random.default_rng(n_branches)
+    T = rng.integers(1, tmax + 1, size=n_branches)
+    S = T + rng.integers(0, smax, size=n_branches)
+    spec = small_spec(h_q=h_q, h_kv=h_kv, page_size=page, prefix_len=prefix, causal=True,
+                      q_rows=[int(x) for x in T], suffix_lens=[int(x) for x in S],
+                      permute_prefix=True, permute_suffix=True, seed=n_branches + 7)
+    w = draw(spec)
+    out, lse = DevWorkload(w).run()
+    compare(out, lse, *oracle_ref(w), what=f"{n_branches} branches")
