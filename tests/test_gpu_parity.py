@@ -169,3 +169,46 @@ def test_many_branches(n_branches, prefix, page, h_q, h_kv, tmax, smax):
     w = draw(spec)
     out, lse = DevWorkload(w).run()
     compare(out, lse, *oracle_ref(w), what=f"{n_branches} branches")
+
+
+def test_pools_beyond_4gb():
+    """K/V pools of 7.9 GB each (60000 pages of 8 KV heads x 64 tokens) with
+    the problem's pages scattered over their last 8000 ids, so that page
+    offsets pass 32-bit byte offsets: attention (the kernel's TMA rows) against
+    the oracle on a compact copy of the same pages, then an append of one row
+    per branch read back through the high page ids."""
+    spec = small_spec(h_q=64, h_kv=8, page_size=64, prefix_len=1024, q_rows=[1, 3, 2, 1],
+                      suffix_lens=[100, 90, 130, 64], permute_prefix=True, permute_suffix=True,
+                      seed=321)
+    w = draw(spec)
+    s = w.spec
+    dw = DevWorkload(w)
+    n_big = 60000
+    remap = (n_big - 8000 + np.random.default_rng(4).permutation(8000)[:w.num_pages])
+    kb = torch.empty((n_big, s.h_kv, s.page_size, s.d), dtype=torch.bfloat16, device="cuda")
+    vb = torch.empty_like(kb)
+    idx = torch.from_numpy(remap.astype(np.int64)).cuda()
+    kb[idx] = dw.k
+    vb[idx] = dw.v
+    tb = dw.table_host.copy()
+    tb[tb >= 0] = remap[tb[tb >= 0]]
+    assert int(tb.max()) * s.h_kv * s.page_size * s.d * 2 > 2**32
+    t_big = torch.from_numpy(tb.astype(np.int32)).cuda()
+    out, lse = dw.run(table=t_big, k=kb, v=vb)
+    compare(out, lse, *oracle_ref(w), what="pools beyond 4 GB")
+    # one new row per branch over its last token (its page is allocated)
+    before = (np.asarray(w.suffix_lens) - 1).astype(np.int32)
+    add = np.ones(len(before), dtype=np.int32)
+    g = torch.Generator().manual_seed(5)
+    k_new = torch.randn((len(before), s.h_kv, s.d), generator=g).to(torch.bfloat16).cuda()
+    v_new = torch.randn((len(before), s.h_kv, s.d), generator=g).to(torch.bfloat16).cuda()
+    binding.kv_append(k_new, v_new, kb, vb, t_big, s.prefix_len, before, add, s.page_size)
+    assert binding.last_error() == binding.OK
+    for b in range(len(before)):
+        pos = s.prefix_len + int(before[b])
+        page = int(tb[b, pos // s.page_size])
+        assert page >= n_big - 8000
+        assert torch.equal(kb[page, :, pos % s.page_size], k_new[b])
+        assert torch.equal(vb[page, :, pos % s.page_size], v_new[b])
+    del kb, vb
+    torch.cuda.empty_cache()
