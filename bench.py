@@ -206,6 +206,25 @@ def gpu_id_for_smi(torch, local_rank: int) -> str:
 
 
 # ------------------------------------------------------------------ oracle leg
+def cpu_model() -> str:
+    """The host CPU's model name (x86 /proc/cpuinfo, else lscpu, else the ISA)."""
+    import platform
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=5).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return platform.machine()
+
+
 def oracle_sample(w, budget_s: float = 15.0):
     """Time the fp64 oracle (as it stands) on a bounded sample of rows of `w`;
     returns (us per full call extrapolated, seconds, rows, threads, repetitions)."""
@@ -267,7 +286,7 @@ def run_reference(args):
 
     def cpu_of(value, info_, what):
         return {"value": value, "unit": "us/call", "cores": info_[3], "kind": "oracle",
-                "sample": f"{info_[2]} of {what.total_rows} query tokens (all heads) "
+                "cpu_model": cpu_model(), "sample": f"{info_[2]} of {what.total_rows} query tokens (all heads) "
                           f"x {info_[4]} repetitions, {info_[1]:.1f} s per step, "
                           f"extrapolated by visible keys"}
 
@@ -559,12 +578,16 @@ class Bench:
         if cpu_budget_s > 0 and int(os.environ.get("RANK", "0")) == 0:
             us, dt, nrows, threads, reps = oracle_sample(w, budget_s=cpu_budget_s)
             cpu = {"value": us, "unit": "us/call", "cores": threads, "kind": "oracle",
+                   "cpu_model": cpu_model(),
                    "sample": f"{nrows} of {R} query tokens (all {s.h_q} heads) x {reps} "
                              f"repetitions, {dt:.1f} s, extrapolated to the full call by "
                              f"visible keys"}
         entry = {
             "value": value_us, "unit": "us/call", "steps": steps,
             "kernel_us": mean_split * 1e3,
+            # medians over the steps (this rank), beside the means above
+            "median_us": float(np.median(call_ms)) * 1e3,
+            "kernel_median_us": float(np.median(split_ms)) * 1e3,
             "config": workload_config(w, self.world),
             "plan": {"work_units": int(len(units)), "persistent_ctas": int(len(cta_first) - 1),
                      "partial_blocks": n_parts},
