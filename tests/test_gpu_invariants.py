@@ -200,3 +200,28 @@ def test_two_threads_on_two_streams():
     assert not errors, errors
     for k, (o, l) in enumerate(refs):
         assert torch.equal(results[k][0], o) and torch.equal(results[k][1], l)
+
+
+@pytest.mark.parametrize("fused", [0, 1], ids=["separate_merge", "fused_merge"])
+def test_without_lse(fused):
+    """lse = NULL (a caller that needs only out): the same out, bit for bit,
+    from the merge (separate and fused) and from units written directly."""
+    specs = [
+        small_spec(h_q=16, h_kv=2, page_size=16, prefix_len=1024, q_rows=[3, 9, 1],
+                   suffix_lens=[200, 45, 700], seed=61),             # split: partials + merge
+        small_spec(h_q=16, h_kv=2, page_size=64, prefix_len=0, q_rows=[300],
+                   suffix_lens=[300], seed=62),                      # one branch: direct units
+    ]
+    try:
+        binding.set_option(binding.OPT_FUSED_MERGE, fused)
+        for spec in specs:
+            dw = DevWorkload(draw(spec))
+            s = dw.w.spec
+            ref_out, _ = dw.run()
+            out, lse = binding.attn(dw.q, dw.k, dw.v, dw.table, s.prefix_len, dw.w.suffix_lens,
+                                    dw.w.q_rows, s.h_q, s.h_kv, s.page_size, s.scale, s.causal,
+                                    want_lse=False)
+            assert lse is None and binding.last_error() == binding.OK
+            assert torch.equal(out, ref_out)
+    finally:
+        binding.set_option(binding.OPT_FUSED_MERGE, 0)

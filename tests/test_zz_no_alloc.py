@@ -133,3 +133,14 @@ def test_noalloc_decode_steps(q_rows):
         ref = oracle.attn(dw.w.q, dw.w.k_pool, dw.w.v_pool, dw.table_host, spec.prefix_len, S,
                           dw.w.q_rows, spec.h_q, spec.h_kv, spec.page_size, spec.scale, spec.causal)
         compare(out, lse, *ref, what=f"no-alloc step +{grow}")
+
+
+def test_noalloc_without_lse():
+    """lse = NULL through the no-allocation entry: out as with lse."""
+    dw = DevWorkload(draw(WORKLOADS["decode"]))
+    ref_out, ref_lse = dw.run()
+    out = torch.full_like(ref_out, float("nan"))
+    assert _noalloc(dw, out, None) == binding.OK
+    assert binding.last_error() == binding.OK
+    d = (out.double() - ref_out.double()).abs()
+    assert d.max().item() <= TOL_MAX_O and d.mean().item() <= TOL_MEAN_O
