@@ -225,3 +225,46 @@ def test_without_lse(fused):
             assert torch.equal(out, ref_out)
     finally:
         binding.set_option(binding.OPT_FUSED_MERGE, 0)
+
+
+def _bf16_bits(x: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16) \
+        .view(torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("causal", [False, True], ids=["noncausal", "causal"])
+def test_lazy_rescale_every_tile(causal):
+    """Scores that rise by about 70 every 128 keys (keys along one direction u
+    with a magnitude growing with their position, queries along u): each tile's
+    row max passes the reference by more than 2^8, so O is rescaled in TMEM on
+    every tile and every split starts from its own reference. Against the
+    oracle on the same bf16 inputs."""
+    import dataclasses
+    spec = small_spec(h_q=16, h_kv=2, page_size=64, prefix_len=1024, q_rows=[2, 5],
+                      suffix_lens=[300, 520], causal=causal, permute_prefix=True,
+                      permute_suffix=True, seed=71)
+    w = draw(spec)
+    s = w.spec
+    d = s.d
+    rng = np.random.default_rng(0)
+    u = rng.standard_normal(d)
+    u /= np.linalg.norm(u)
+    R = w.total_rows
+    q = 8.0 * u[None, None, :] + 0.1 * rng.standard_normal((R, s.h_q, d))
+    table = oracle.fork(w.prefix_pages, w.suffix_lens, s.page_size, w.free_pages,
+                        w.max_pages_per_branch)
+    k = w.k_pool.copy()
+    # the shared prefix pages hold one set of keys for every branch
+    noise_prefix = 0.1 * rng.standard_normal((s.h_kv, s.prefix_len, d))
+    for b in range(w.num_branches):
+        n = s.prefix_len + int(w.suffix_lens[b])
+        j = np.arange(n)
+        base = (70.0 / (128 * 8.0)) * j[:, None] * u[None, :]          # score ~ 0.55 j
+        for h in range(s.h_kv):
+            vals = base.copy()
+            vals[:s.prefix_len] += noise_prefix[h]
+            vals[s.prefix_len:] += 0.1 * rng.standard_normal((n - s.prefix_len, d))
+            k[table[b, j // s.page_size], h, j % s.page_size, :] = _bf16_bits(vals)
+    w2 = dataclasses.replace(w, q=_bf16_bits(q), k_pool=k)
+    out, lse = DevWorkload(w2).run()
+    compare(out, lse, *oracle_ref(w2), what=f"rescale every tile, causal={causal}")
