@@ -6,6 +6,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from shared_prefix_fan_gb300 import binding
 from shared_prefix_fan_gb300.workloads import WORKLOADS, draw, small_spec
 from tests.gpu_helpers import DevWorkload, compare, oracle_ref, sample_rows
@@ -212,3 +213,22 @@ def test_pools_beyond_4gb():
         assert torch.equal(vb[page, :, pos % s.page_size], v_new[b])
     del kb, vb
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("scale", [1e-3, 0.5, 2.0])
+def test_softmax_scale(scale):
+    """Softmax scales other than 1/sqrt(d): nearly uniform weights (1e-3) and
+    sharply peaked ones (2.0, scores up to ~100 in base-2 units), on a split
+    problem with causal suffixes, against the oracle with the same scale."""
+    spec = small_spec(h_q=16, h_kv=2, page_size=32, prefix_len=768, q_rows=[4, 7, 1],
+                      suffix_lens=[150, 60, 400], permute_prefix=True, permute_suffix=True,
+                      seed=88)
+    w = draw(spec)
+    s = w.spec
+    dw = DevWorkload(w)
+    out, lse = binding.attn(dw.q, dw.k, dw.v, dw.table, s.prefix_len, w.suffix_lens, w.q_rows,
+                            s.h_q, s.h_kv, s.page_size, scale, s.causal)
+    assert binding.last_error() == binding.OK
+    ref = oracle.attn(w.q, w.k_pool, w.v_pool, dw.table_host, s.prefix_len, w.suffix_lens,
+                      w.q_rows, s.h_q, s.h_kv, s.page_size, scale, s.causal)
+    compare(out, lse, *ref, what=f"scale {scale}")
