@@ -29,6 +29,7 @@ import subprocess
 import sys
 import tempfile
 import time
+import types
 
 import numpy as np
 
@@ -122,6 +123,11 @@ def workload_config(w, world: int) -> dict:
             "prefix_len": s.prefix_len, "suffix_tokens": int(w.suffix_lens.sum()),
             "page_size": s.page_size, "causal": s.causal, "l2": L2_NOTE,
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+
+def host_bf16(torch, bits):
+    """A host bf16 tensor over uint16 bf16 bits (no copy)."""
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
 
 
 def new_token_rows(w, table):
@@ -396,44 +402,47 @@ class Bench:
     def max_ranks(self, vals):
         return max_over_ranks(vals, self.dist if self.world > 1 else None, "cuda")
 
-    def run(self, name, steps, warmup, soak_s, e2e_steps, cpu_budget_s):
+    def _check(self, name):
+        rc = self.binding.last_error()
+        if rc != self.binding.OK:
+            raise RuntimeError(f"{name}: device error {self.binding.strerror(rc)}")
+
+    def _prepare(self, name):
+        """The workload `name` drawn, its page table forked, host copies of its
+        inputs and resident device copies, out / lse, and the timed call."""
         torch, binding = self.torch, self.binding
-        w = draw(WORKLOADS[name])
-        s = w.spec
-        table = binding.fork(w.prefix_pages, w.suffix_lens, s.page_size, w.free_pages,
-                             w.max_pages_per_branch)
-
-        def host_bf16(bits):
-            return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
-
-        h_q, h_k, h_v = host_bf16(w.q), host_bf16(w.k_pool), host_bf16(w.v_pool)
-        h_t = torch.from_numpy(table)
-        q, k, v, t = (x.cuda() for x in (h_q, h_k, h_v, h_t))
-        R = w.total_rows
-        out = torch.empty((R, s.h_q, s.d), dtype=torch.float32, device="cuda")
-        lse = torch.empty((R, s.h_q), dtype=torch.float32, device="cuda")
+        c = types.SimpleNamespace(name=name)
+        c.w = w = draw(WORKLOADS[name])
+        c.s = s = w.spec
+        c.table = binding.fork(w.prefix_pages, w.suffix_lens, s.page_size, w.free_pages,
+                               w.max_pages_per_branch)
+        c.h_q, c.h_k, c.h_v = (host_bf16(torch, x) for x in (w.q, w.k_pool, w.v_pool))
+        c.h_t = torch.from_numpy(c.table)
+        c.q, c.k, c.v, c.t = (x.cuda() for x in (c.h_q, c.h_k, c.h_v, c.h_t))
+        c.out = torch.empty((w.total_rows, s.h_q, s.d), dtype=torch.float32, device="cuda")
+        c.lse = torch.empty((w.total_rows, s.h_q), dtype=torch.float32, device="cuda")
 
         def call():
-            binding.attn(q, k, v, t, s.prefix_len, w.suffix_lens, w.q_rows, s.h_q, s.h_kv,
-                         s.page_size, s.scale, s.causal, out=out, lse=lse)
+            binding.attn(c.q, c.k, c.v, c.t, s.prefix_len, w.suffix_lens, w.q_rows, s.h_q,
+                         s.h_kv, s.page_size, s.scale, s.causal, out=c.out, lse=c.lse)
 
+        c.call = call
+        return c
+
+    def _time_calls(self, c, steps, warmup, soak_s):
+        """Warm-up, an untimed soak (clocks settle and are sampled), then the
+        timed steps: (call ms per step, attention-kernel ms per step, clocks)."""
+        torch, binding = self.torch, self.binding
         for _ in range(max(3, warmup)):
             self.flush_l2()
-            call()
+            c.call()
         torch.cuda.synchronize()
-        rc = binding.last_error()
-        if rc != binding.OK:
-            raise RuntimeError(f"{name}: device error {binding.strerror(rc)}")
-        units, cta_first, n_parts = binding.plan(
-            w.suffix_lens, w.q_rows, s.prefix_len, s.h_q, s.h_kv, s.page_size, s.causal,
-            self.sms)
-        launches_per_call = 1 + (1 if n_parts > 0 else 0)
-
+        self._check(c.name)
         sampler = ClockSampler(gpu_id_for_smi(torch, self.local))
         t_end = time.perf_counter() + soak_s
-        while time.perf_counter() < t_end:   # untimed soak: clocks settle and get sampled
+        while time.perf_counter() < t_end:
             self.flush_l2()
-            call()
+            c.call()
             torch.cuda.synchronize()
         stream = torch.cuda.current_stream()
         ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4)) for _ in range(steps)]
@@ -453,114 +462,132 @@ class Bench:
         for e0, e1, k0, k1 in ev:
             self.flush_l2()                    # L2 flushed between timed calls
             e0.record(stream)
-            call()
+            c.call()
             e1.record(stream)
             self.flush_l2()
             binding.set_profile_events(k0, k1)  # brackets the split-KV kernel alone
-            call()
+            c.call()
             binding.set_profile_events(None, None)
         torch.cuda.synchronize()
         if self.world > 1:
             self.dist.barrier()
         clocks = sampler.stop()
+        self._check(c.name)
         call_ms = np.array([a.elapsed_time(b) for a, b, _, _ in ev])
         split_ms = np.array([a.elapsed_time(b) for _, _, a, b in ev])
-        rc = binding.last_error()
-        if rc != binding.OK:
-            raise RuntimeError(f"{name}: device error {binding.strerror(rc)}")
-        mean_call, mean_split = self.max_ranks([float(call_ms.mean()), float(split_ms.mean())])
+        return call_ms, split_ms, clocks
 
-        # end to end: inputs from pinned host memory, result read back, every step
-        e2e = None
-        if e2e_steps > 0:
-            p_q, p_k, p_v, p_t = (x.pin_memory() for x in (h_q, h_k, h_v, h_t))
-            p_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-            p_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-            e2e_ms = []
-            for i in range(e2e_steps + 2):
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                self.flush_l2()
-                a.record(stream)
-                q.copy_(p_q, non_blocking=True)
-                k.copy_(p_k, non_blocking=True)
-                v.copy_(p_v, non_blocking=True)
-                t.copy_(p_t, non_blocking=True)
-                call()
-                p_out.copy_(out, non_blocking=True)
-                p_lse.copy_(lse, non_blocking=True)
-                b.record(stream)
-                torch.cuda.synchronize()
-                if i >= 2:
-                    e2e_ms.append(a.elapsed_time(b))
-            e2e_val = self.max_ranks([float(np.mean(e2e_ms)) * 1e3])[0]
-            h2d = sum(x.numel() * x.element_size() for x in (p_q, p_k, p_v, p_t))
-            d2h = sum(x.numel() * x.element_size() for x in (p_out, p_lse))
-            e2e = {"value": e2e_val, "unit": "us/call", "h2d_bytes_per_step": int(h2d),
-                   "d2h_bytes_per_step": int(d2h), "steps": e2e_steps,
-                   "note": "q, K/V page pool and page table copied from pinned host memory, "
-                           "out and lse copied back, every step"}
-            # A decode loop keeps the cache in HBM: each step brings only the
-            # queries and the new tokens' K/V rows, appends the rows to the
-            # pools, attends, and reads the result back. The appended rows
-            # are the ones already at those positions, so the pools and the
-            # result stay as above.
-            T = np.asarray(w.q_rows, dtype=np.int64)
-            S = np.asarray(w.suffix_lens, dtype=np.int64)
-            pages, slot = new_token_rows(w, table)
-            k_rows = host_bf16(w.k_pool[pages, :, slot, :])   # [R, H_kv, d]
-            v_rows = host_bf16(w.v_pool[pages, :, slot, :])
-            # One staging buffer each way (one copy per direction per step):
-            # q, the new K and V rows and the page table up; out and lse down.
-            ups = [h_q, k_rows, v_rows, h_t]
-            offs, n = [], 0
-            for x in ups:
-                offs.append(n)
-                n += (x.numel() * x.element_size() + 255) // 256 * 256
-            p_up = torch.empty(n, dtype=torch.uint8).pin_memory()
-            d_up = torch.empty(n, dtype=torch.uint8, device="cuda")
+    def _timed_steps(self, steps, body):
+        """Mean µs (max over ranks) of `body` per step, events around it, the L2
+        flushed before each step, two untimed steps first."""
+        torch = self.torch
+        stream = torch.cuda.current_stream()
+        ms = []
+        for i in range(steps + 2):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            self.flush_l2()
+            a.record(stream)
+            body()
+            b.record(stream)
+            torch.cuda.synchronize()
+            if i >= 2:
+                ms.append(a.elapsed_time(b))
+        return self.max_ranks([float(np.mean(ms)) * 1e3])[0]
 
-            def section(buf, i):
-                x = ups[i]
-                nb = x.numel() * x.element_size()
-                return buf[offs[i]:offs[i] + nb].view(x.dtype).view(x.shape)
+    def _e2e_full(self, c, steps):
+        """End to end: q, the K/V pools and the page table from pinned host
+        memory, the call, out and lse read back, every step."""
+        torch = self.torch
+        p_q, p_k, p_v, p_t = (x.pin_memory() for x in (c.h_q, c.h_k, c.h_v, c.h_t))
+        p_out = torch.empty(c.out.shape, dtype=c.out.dtype).pin_memory()
+        p_lse = torch.empty(c.lse.shape, dtype=c.lse.dtype).pin_memory()
 
-            for i, x in enumerate(ups):
-                section(p_up, i).copy_(x)
-            dq, dkn, dvn, dt = (section(d_up, i) for i in range(4))
-            n_out = out.numel()
-            d_down = torch.empty(n_out + lse.numel(), dtype=torch.float32, device="cuda")
-            p_down = torch.empty(d_down.shape, dtype=torch.float32).pin_memory()
-            out2, lse2 = d_down[:n_out].view(out.shape), d_down[n_out:].view(lse.shape)
-            before = (S - T).astype(np.int32)
-            res_ms = []
-            for i in range(e2e_steps + 2):
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                self.flush_l2()
-                a.record(stream)
-                d_up.copy_(p_up, non_blocking=True)
-                binding.kv_append(dkn, dvn, k, v, dt, s.prefix_len, before, w.q_rows,
-                                  s.page_size)
-                binding.attn(dq, k, v, dt, s.prefix_len, w.suffix_lens, w.q_rows, s.h_q,
-                             s.h_kv, s.page_size, s.scale, s.causal, out=out2, lse=lse2)
-                p_down.copy_(d_down, non_blocking=True)
-                b.record(stream)
-                torch.cuda.synchronize()
-                if i >= 2:
-                    res_ms.append(a.elapsed_time(b))
-            rc = binding.last_error()
-            if rc != binding.OK:
-                raise RuntimeError(f"{name}: device error {binding.strerror(rc)}")
-            # the rows went back where they came from: same pools, same result
-            if not (torch.equal(out2, out) and torch.equal(lse2, lse)):
-                raise RuntimeError(f"{name}: the resident-cache step changed the result")
-            res_val = self.max_ranks([float(np.mean(res_ms)) * 1e3])[0]
-            e2e["resident_cache"] = {
-                "value": res_val, "unit": "us/call", "h2d_bytes_per_step": int(p_up.numel()),
-                "d2h_bytes_per_step": int(p_down.numel() * 4), "steps": e2e_steps,
+        def step():
+            c.q.copy_(p_q, non_blocking=True)
+            c.k.copy_(p_k, non_blocking=True)
+            c.v.copy_(p_v, non_blocking=True)
+            c.t.copy_(p_t, non_blocking=True)
+            c.call()
+            p_out.copy_(c.out, non_blocking=True)
+            p_lse.copy_(c.lse, non_blocking=True)
+
+        value = self._timed_steps(steps, step)
+        h2d = sum(x.numel() * x.element_size() for x in (p_q, p_k, p_v, p_t))
+        d2h = sum(x.numel() * x.element_size() for x in (p_out, p_lse))
+        return {"value": value, "unit": "us/call", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h), "steps": steps,
+                "note": "q, K/V page pool and page table copied from pinned host memory, "
+                        "out and lse copied back, every step"}
+
+    def _e2e_resident(self, c, steps):
+        """A decode loop keeps the cache in HBM: each step brings only the
+        queries and the new tokens' K/V rows, appends the rows to the pools,
+        attends, and reads the result back. The appended rows are the ones
+        already at those positions, so the pools and the result stay as in
+        the timed calls (checked bit for bit)."""
+        torch, binding = self.torch, self.binding
+        w, s = c.w, c.s
+        T = np.asarray(w.q_rows, dtype=np.int64)
+        S = np.asarray(w.suffix_lens, dtype=np.int64)
+        pages, slot = new_token_rows(w, c.table)
+        k_rows = host_bf16(torch, w.k_pool[pages, :, slot, :])   # [R, H_kv, d]
+        v_rows = host_bf16(torch, w.v_pool[pages, :, slot, :])
+        # One staging buffer each way (one copy per direction per step):
+        # q, the new K and V rows and the page table up; out and lse down.
+        ups = [c.h_q, k_rows, v_rows, c.h_t]
+        offs, n = [], 0
+        for x in ups:
+            offs.append(n)
+            n += (x.numel() * x.element_size() + 255) // 256 * 256
+        p_up = torch.empty(n, dtype=torch.uint8).pin_memory()
+        d_up = torch.empty(n, dtype=torch.uint8, device="cuda")
+
+        def section(buf, i):
+            x = ups[i]
+            nb = x.numel() * x.element_size()
+            return buf[offs[i]:offs[i] + nb].view(x.dtype).view(x.shape)
+
+        for i, x in enumerate(ups):
+            section(p_up, i).copy_(x)
+        dq, dkn, dvn, dt = (section(d_up, i) for i in range(4))
+        n_out = c.out.numel()
+        d_down = torch.empty(n_out + c.lse.numel(), dtype=torch.float32, device="cuda")
+        p_down = torch.empty(d_down.shape, dtype=torch.float32).pin_memory()
+        out2, lse2 = d_down[:n_out].view(c.out.shape), d_down[n_out:].view(c.lse.shape)
+        before = (S - T).astype(np.int32)
+
+        def step():
+            d_up.copy_(p_up, non_blocking=True)
+            binding.kv_append(dkn, dvn, c.k, c.v, dt, s.prefix_len, before, w.q_rows,
+                              s.page_size)
+            binding.attn(dq, c.k, c.v, dt, s.prefix_len, w.suffix_lens, w.q_rows, s.h_q,
+                         s.h_kv, s.page_size, s.scale, s.causal, out=out2, lse=lse2)
+            p_down.copy_(d_down, non_blocking=True)
+
+        value = self._timed_steps(steps, step)
+        self._check(c.name)
+        if not (torch.equal(out2, c.out) and torch.equal(lse2, c.lse)):
+            raise RuntimeError(f"{c.name}: the resident-cache step changed the result")
+        return {"value": value, "unit": "us/call", "h2d_bytes_per_step": int(p_up.numel()),
+                "d2h_bytes_per_step": int(p_down.numel() * 4), "steps": steps,
                 "note": "K/V pools resident; q, the step's new K/V rows and the page table "
                         "copied up from one pinned staging buffer, fanout_kv_append, the "
                         "call, out and lse copied down in one copy, every step"}
-            del p_q, p_k, p_v, p_t, p_out, p_lse, p_up, d_up, d_down, p_down
+
+    def run(self, name, steps, warmup, soak_s, e2e_steps, cpu_budget_s):
+        """One workload's entry of the JSON line."""
+        c = self._prepare(name)
+        w, s = c.w, c.s
+        units, cta_first, n_parts = self.binding.plan(
+            w.suffix_lens, w.q_rows, s.prefix_len, s.h_q, s.h_kv, s.page_size, s.causal,
+            self.sms)
+        launches_per_call = 1 + (1 if n_parts > 0 else 0)
+        call_ms, split_ms, clocks = self._time_calls(c, steps, warmup, soak_s)
+        mean_call, mean_split = self.max_ranks([float(call_ms.mean()), float(split_ms.mean())])
+        e2e = None
+        if e2e_steps > 0:
+            e2e = self._e2e_full(c, e2e_steps)
+            e2e["resident_cache"] = self._e2e_resident(c, e2e_steps)
 
         work = algorithmic_work(w)
         peaks = load_peaks()
@@ -579,9 +606,9 @@ class Bench:
             us, dt, nrows, threads, reps = oracle_sample(w, budget_s=cpu_budget_s)
             cpu = {"value": us, "unit": "us/call", "cores": threads, "kind": "oracle",
                    "cpu_model": cpu_model(),
-                   "sample": f"{nrows} of {R} query tokens (all {s.h_q} heads) x {reps} "
-                             f"repetitions, {dt:.1f} s, extrapolated to the full call by "
-                             f"visible keys"}
+                   "sample": f"{nrows} of {w.total_rows} query tokens (all {s.h_q} heads) x "
+                             f"{reps} repetitions, {dt:.1f} s, extrapolated to the full call "
+                             f"by visible keys"}
         entry = {
             "value": value_us, "unit": "us/call", "steps": steps,
             "kernel_us": mean_split * 1e3,
@@ -598,8 +625,8 @@ class Bench:
             # the timed region holds each step's timed call and its kernel-only twin
             "gpu_launches": 2 * launches_per_call * steps, "clocks": clocks,
         }
-        del q, k, v, t, out, lse
-        torch.cuda.empty_cache()
+        c.__dict__.clear()   # the call closure refers to c: drop the tensors now
+        self.torch.cuda.empty_cache()
         return entry
 
 
