@@ -675,9 +675,17 @@ def main():
     for name in names:
         if name == args.config:
             continue
-        per[name] = bench.run(name, args.steps, args.warmup, min(args.soak_s, 0.5),
-                              0 if args.no_e2e else max(3, min(args.steps, 10)),
-                              0.0 if args.no_cpu_baseline else 6.0)
+        try:
+            per[name] = bench.run(name, args.steps, args.warmup, min(args.soak_s, 0.5),
+                                  0 if args.no_e2e else max(3, min(args.steps, 10)),
+                                  0.0 if args.no_cpu_baseline else 6.0)
+        except (RuntimeError, MemoryError) as e:
+            # one process: the line still carries the other workloads and the
+            # error; with several ranks a rank that stopped early would leave
+            # the others waiting in a barrier, so every rank stops
+            if world > 1:
+                raise
+            per[name] = {"error": f"{type(e).__name__}: {e}"}
 
     line = {
         "metric": METRIC, "value": head["value"], "unit": "us/call", "n_gpus": world,
