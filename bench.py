@@ -512,6 +512,7 @@ class Bench:
             p_lse.copy_(c.lse, non_blocking=True)
 
         value = self._timed_steps(steps, step)
+        self._check(c.name)
         h2d = sum(x.numel() * x.element_size() for x in (p_q, p_k, p_v, p_t))
         d2h = sum(x.numel() * x.element_size() for x in (p_out, p_lse))
         return {"value": value, "unit": "us/call", "h2d_bytes_per_step": int(h2d),
