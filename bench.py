@@ -577,6 +577,34 @@ class Bench:
                         "copied up from one pinned staging buffer, fanout_kv_append, the "
                         "call, out and lse copied down in one copy, every step"}
 
+    def _kv_append(self, c, steps):
+        """The cache append of the workload's new tokens (fanout_kv_append, the
+        step before attention in a decode loop): every query token's own K and
+        V rows written into its page and slot, timed alone like the call. The
+        rows written are the bytes already there, so the pools do not change.
+        Algorithmic bytes: the new rows read once and written once."""
+        torch, binding = self.torch, self.binding
+        w, s = c.w, c.s
+        T = np.asarray(w.q_rows, dtype=np.int64)
+        S = np.asarray(w.suffix_lens, dtype=np.int64)
+        pages, slot = new_token_rows(w, c.table)
+        kn = host_bf16(torch, w.k_pool[pages, :, slot, :]).cuda()
+        vn = host_bf16(torch, w.v_pool[pages, :, slot, :]).cuda()
+        before = (S - T).astype(np.int32)
+
+        def step():
+            binding.kv_append(kn, vn, c.k, c.v, c.t, s.prefix_len, before, w.q_rows,
+                              s.page_size)
+
+        value = self._timed_steps(steps, step)
+        self._check(c.name)
+        nbytes = 2 * (kn.numel() + vn.numel()) * kn.element_size()
+        peak = load_peaks()["hbm"]
+        achieved = nbytes / (value * 1e-6) / 1e9
+        return {"value": value, "unit": "us/call", "rows": int(w.total_rows),
+                "algorithmic_bytes": int(nbytes), "achieved_gbs": achieved,
+                "peak_gbs": peak, "frac": achieved / peak, "steps": steps}
+
     def run(self, name, steps, warmup, soak_s, e2e_steps, cpu_budget_s):
         """One workload's entry of the JSON line."""
         c = self._prepare(name)
@@ -591,6 +619,7 @@ class Bench:
         if e2e_steps > 0:
             e2e = self._e2e_full(c, e2e_steps)
             e2e["resident_cache"] = self._e2e_resident(c, e2e_steps)
+        append = self._kv_append(c, min(steps, 20))
 
         work = algorithmic_work(w)
         peaks = load_peaks()
@@ -624,7 +653,7 @@ class Bench:
             "call_roofline": {"t_roof_us": t_call_roof * 1e6,
                               "frac": t_call_roof / (value_us * 1e-6),
                               "bytes": work["call_bytes"], "flops": work["flops"]},
-            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "kv_append": append,
             # the timed region holds each step's timed call and its kernel-only twin
             "gpu_launches": 2 * launches_per_call * steps, "clocks": clocks,
         }
