@@ -65,3 +65,39 @@ def test_kv_append_skips_bad_page_ids():
     binding.kv_append(k_new, k_new.clone(), k_pool, v_pool, table, 0, [16], [1], 16)
     assert binding.last_error() == binding.EINVAL
     assert (k_pool == 0).all() and (v_pool == 0).all()
+
+
+@pytest.mark.parametrize("ps", [64, 24])
+def test_kv_append_many_rows(ps):
+    """A long append (4 branches x 700 new tokens, 8 KV heads: several items per
+    warp) lands every row where the oracle's append puts it, bit for bit, for a
+    power-of-two page and for one that is not (24 tokens)."""
+    ensure_lib()
+    rng = np.random.default_rng(ps)
+    B, hkv, d = 4, 8, 128
+    s_old = rng.integers(0, 300, size=B).astype(np.int32)
+    add = np.full(B, 700, dtype=np.int32)
+    P = 2 * ps
+    ends = P + s_old + add
+    mp = int(((ends + ps - 1) // ps).max())
+    n_pages = B * mp + 8
+    perm = rng.permutation(n_pages).astype(np.int32)
+    table = np.full((B, mp), -1, dtype=np.int32)
+    n_pre, nxt = P // ps, P // ps
+    for b in range(B):
+        need = int((ends[b] + ps - 1) // ps)
+        table[b, :n_pre] = perm[:n_pre]                    # the shared prefix pages
+        table[b, n_pre:need] = perm[nxt:nxt + need - n_pre]
+        nxt += need - n_pre
+    kp = rng.integers(0, 2**16, size=(n_pages, hkv, ps, d), dtype=np.uint16)
+    vp = rng.integers(0, 2**16, size=(n_pages, hkv, ps, d), dtype=np.uint16)
+    R = int(add.sum())
+    kn = rng.integers(0, 2**16, size=(R, hkv, d), dtype=np.uint16)
+    vn = rng.integers(0, 2**16, size=(R, hkv, d), dtype=np.uint16)
+    rk, rv = oracle.kv_append(kn, vn, kp, vp, table, P, s_old, add)
+    gk, gv = to_dev_bf16(kp), to_dev_bf16(vp)
+    binding.kv_append(to_dev_bf16(kn), to_dev_bf16(vn), gk, gv, torch.from_numpy(table).cuda(),
+                      P, s_old, add, ps)
+    assert binding.last_error() == binding.OK
+    assert np.array_equal(gk.view(torch.int16).cpu().numpy().view(np.uint16), rk)
+    assert np.array_equal(gv.view(torch.int16).cpu().numpy().view(np.uint16), rv)
