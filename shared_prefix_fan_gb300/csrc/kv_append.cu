@@ -35,15 +35,24 @@ __global__ void __launch_bounds__(256)
     const int64_t n_items = static_cast<int64_t>(p.R) * p.H_kv;
     const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
     const int chunks = p.d / 8;  // 16-byte pieces per row
-    // Index arithmetic in 32 bits and shifts where it can be: 64-bit divisions
-    // per item made this scatter bound by instruction issue, not by memory.
+    // Index arithmetic in 32 bits, and shifts for power-of-two head counts and
+    // page sizes (warp-uniform branches): 64-bit divisions per item made this
+    // scatter bound by instruction issue, not by memory.
+    const bool hkv_pow2 = (p.H_kv & (p.H_kv - 1)) == 0;
+    const int hkv_shift = __ffs(p.H_kv) - 1;
     const bool ps_pow2 = (p.page_size & (p.page_size - 1)) == 0;
     const int ps_shift = __ffs(p.page_size) - 1;
     for (int64_t item = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
          item < n_items; item += warps) {
         const int32_t it = static_cast<int32_t>(item);  // R * H_kv <= 2^31 (host check)
-        const int32_t r = it / p.H_kv;
-        const int32_t h = it - r * p.H_kv;
+        int32_t r, h;
+        if (hkv_pow2) {
+            r = it >> hkv_shift;
+            h = it & (p.H_kv - 1);
+        } else {
+            r = it / p.H_kv;
+            h = it - r * p.H_kv;
+        }
         // branch of row r: largest b with row_off[b] <= r (binary search)
         int lo = 0, hi = p.num_branches - 1;
         while (lo < hi) {
@@ -52,8 +61,14 @@ __global__ void __launch_bounds__(256)
         }
         const int b = lo;
         const int64_t pos = static_cast<int64_t>(p.prefix_len) + p.suffix_len[b] + (r - p.row_off[b]);
-        const int64_t pidx = ps_pow2 ? (pos >> ps_shift) : pos / p.page_size;
-        const int64_t slot = ps_pow2 ? (pos & (p.page_size - 1)) : pos % p.page_size;
+        int64_t pidx, slot;
+        if (ps_pow2) {
+            pidx = pos >> ps_shift;
+            slot = pos & (p.page_size - 1);
+        } else {
+            pidx = pos / p.page_size;
+            slot = pos - pidx * p.page_size;
+        }
         const int32_t page = page_table[static_cast<int64_t>(b) * p.max_pages + pidx];
         if (page < 0 || page >= p.num_pages) {  // never write through a bad page id
             if (lane == 0) atomicCAS(err, 0, 1);

@@ -67,14 +67,14 @@ def test_kv_append_skips_bad_page_ids():
     assert (k_pool == 0).all() and (v_pool == 0).all()
 
 
-@pytest.mark.parametrize("ps", [64, 24])
-def test_kv_append_many_rows(ps):
-    """A long append (4 branches x 700 new tokens, 8 KV heads: several items per
-    warp) lands every row where the oracle's append puts it, bit for bit, for a
-    power-of-two page and for one that is not (24 tokens)."""
+@pytest.mark.parametrize("ps,hkv", [(64, 8), (24, 8), (64, 3), (24, 3)])
+def test_kv_append_many_rows(ps, hkv):
+    """A long append (4 branches x 700 new tokens: several items per warp) lands
+    every row where the oracle's append puts it, bit for bit, for power-of-two
+    and other page sizes (24 tokens) and KV head counts (3)."""
     ensure_lib()
-    rng = np.random.default_rng(ps)
-    B, hkv, d = 4, 8, 128
+    rng = np.random.default_rng(ps * 10 + hkv)
+    B, d = 4, 128
     s_old = rng.integers(0, 300, size=B).astype(np.int32)
     add = np.full(B, 700, dtype=np.int32)
     P = 2 * ps
