@@ -101,3 +101,50 @@ def test_kv_append_many_rows(ps, hkv):
     assert binding.last_error() == binding.OK
     assert np.array_equal(gk.view(torch.int16).cpu().numpy().view(np.uint16), rk)
     assert np.array_equal(gv.view(torch.int16).cpu().numpy().view(np.uint16), rv)
+
+
+def test_decode_loop_with_page_growth():
+    """Six decode steps of a three-branch fan-out, as a caller runs them: grow
+    the tables (fanout_extend, new pages as suffixes cross 16-token pages),
+    append the new tokens' K/V (fanout_kv_append), attend with those tokens as
+    the queries. Every step's tables, pools and attention against the oracle
+    doing the same steps."""
+    ensure_lib()
+    P, ps, hq, hkv = 128, 16, 16, 2
+    s0 = np.array([14, 30, 5], dtype=np.int32)
+    steps = [np.array(a, dtype=np.int32) for a in ([1, 2, 1], [1, 2, 3], [2, 1, 1],
+                                                     [1, 1, 1], [3, 2, 1], [1, 2, 2])]
+    s_final = s0 + sum(steps)
+    spec = small_spec(h_q=hq, h_kv=hkv, page_size=ps, prefix_len=P, q_rows=[1, 1, 1],
+                      suffix_lens=[int(x) for x in s_final], permute_prefix=True,
+                      permute_suffix=True, seed=404)
+    w = draw(spec)        # a pool with pages for the final lengths
+    rng = np.random.default_rng(404)
+    mp = w.max_pages_per_branch
+    n_used0 = sum(-(-int(s) // ps) for s in s0)
+    table = binding.fork(w.prefix_pages, s0, ps, w.free_pages, mp)
+    ref_table = oracle.fork(w.prefix_pages, s0, ps, w.free_pages, mp)
+    free = w.free_pages[n_used0:]
+    k_pool, v_pool = to_dev_bf16(w.k_pool), to_dev_bf16(w.v_pool)
+    rk, rv = w.k_pool.copy(), w.v_pool.copy()
+    s = s0.copy()
+    for i, add in enumerate(steps):
+        R = int(add.sum())
+        kn = _bf16_bits(torch.from_numpy(rng.standard_normal((R, hkv, 128)).astype(np.float32)))
+        vn = _bf16_bits(torch.from_numpy(rng.standard_normal((R, hkv, 128)).astype(np.float32)))
+        q = _bf16_bits(torch.from_numpy(rng.standard_normal((R, hq, 128)).astype(np.float32)))
+        table, used = binding.extend(table, P, s, add, ps, free)
+        ref_table, ref_used = oracle.extend(ref_table, P, s, add, ps, free)
+        assert np.array_equal(table, ref_table) and used == ref_used
+        free = free[used:]
+        t_dev = torch.from_numpy(table).cuda()
+        binding.kv_append(to_dev_bf16(kn), to_dev_bf16(vn), k_pool, v_pool, t_dev, P, s, add, ps)
+        assert binding.last_error() == binding.OK
+        rk, rv = oracle.kv_append(kn, vn, rk, rv, ref_table, P, s, add)
+        s = s + add
+        out, lse = binding.attn(to_dev_bf16(q), k_pool, v_pool, t_dev, P, s, add, hq, hkv, ps,
+                                spec.scale, True)
+        assert binding.last_error() == binding.OK
+        ro, rl = oracle.attn(q, rk, rv, ref_table, P, s, add, hq, hkv, ps, spec.scale, True)
+        compare(out, lse, ro, rl, what=f"decode loop step {i}")
+    assert np.array_equal(k_pool.view(torch.int16).cpu().numpy().view(np.uint16), rk)
