@@ -153,8 +153,10 @@ FANOUT_API int fanout_extend(int32_t *page_table, int32_t num_branches,
  *   k_pages, v_pages  dev bf16 [num_pages][H_kv][page_size][d], written.
  *   page_table        dev int32 [B][max_pages_per_branch] (grown already, e.g.
  *                     by fanout_extend then copied to the device).
- * num_branches <= 1024. An out-of-range page id is never written through: the
- * row is skipped and fanout_last_error() reports FANOUT_EINVAL.
+ * num_branches <= 1024 and (sum of add_lens) * H_kv <= 2^31, else
+ * FANOUT_EUNSUPPORTED; d % 8 == 0 and d <= 1024, else FANOUT_EUNSUPPORTED. An
+ * out-of-range page id is never written through: the row is skipped and
+ * fanout_last_error() reports FANOUT_EINVAL.
  */
 FANOUT_API int fanout_kv_append(const void *k_new, const void *v_new, void *k_pages,
                 void *v_pages, const int32_t *page_table, int32_t prefix_len,
