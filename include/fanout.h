@@ -206,6 +206,10 @@ FANOUT_API int fanout_kv_append(const void *k_new, const void *v_new, void *k_pa
  * row 0. Host-side validation reads only host arrays; page-table entries are read by
  * the kernel (set option FANOUT_OPT_VALIDATE_TABLE to check them on the host
  * with a device-to-host copy first). R == 0 is a no-op returning FANOUT_OK.
+ * Limits: prefix_len + suffix_lens[b] <= 2^29 keys and R * H_q <= 2^24
+ * (FANOUT_EUNSUPPORTED otherwise); max_pages_per_branch must cover
+ * ceil((prefix_len + suffix_lens[b]) / page_size) entries for every branch,
+ * and a branch with query rows must have at least one key (FANOUT_EINVAL).
  * The library keeps a grow-only device workspace per (device, stream) for
  * split partials and the work plan; it is freed by fanout_release().
  */
