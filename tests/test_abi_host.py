@@ -87,6 +87,8 @@ def test_attn_rejects_bad_arguments_on_host(lib):
     assert _attn_rc(lib, scale=0.0) == E
     assert _attn_rc(lib, scale=-0.1) == E
     assert _attn_rc(lib, P=0, S=[0, 4], T=[1, 1], causal=0) == E  # a row with no key
+    assert _attn_rc(lib, S=[1 << 29, 2]) == U      # more than 2^29 keys in a branch
+    assert _attn_rc(lib, T=[1 << 21, 2], S=[1 << 21, 2], causal=0) == U   # R * H_q > 2^24
     # nothing to do is not an error, and needs no device
     assert _attn_rc(lib, T=[0, 0], q=None, out=None) == binding.OK
 
