@@ -49,6 +49,7 @@ def test_noalloc_matches_fanout_attn_on_two_calls():
         compare(out, lse, *oracle_ref(dw.w), what=f"no-alloc {name}")
 
 
+@pytest.mark.filterwarnings("ignore:The CUDA Graph is empty")   # nothing was captured: the point
 def test_noalloc_refuses_a_capturing_stream():
     """Each call copies its plan into the array from host memory that lives
     only for the call, so a call on a stream being captured is refused with
